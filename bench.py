@@ -1,0 +1,469 @@
+"""Benchmark of the stochastic verification step on GB300.
+
+One step = one pass of the verification hot path over one batch: the fused
+max / log-sum-exp / argmax row reduction, the temperature / top-k / top-p /
+min-p filtered Gumbel-max sampler, the point-mass rejection chain with
+replacement / bonus tokens, and the fused per-position prefix-acceptance
+counters -- one spec_verify_sample call on the mixed-temperature workload
+B=128 requests, k=4 draft tokens (640 packed rows), V=152064, bf16.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank verifies its own
+batch (independent requests: weak scaling, no data-path collective).
+`--impl reference` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "verified rows/s and achieved HBM GB/s (% of peak) at B=128,k=4,V=152064 bf16"
+WORKLOAD = ("stochastic verify: B=128, k=4 (640 packed rows), V=152064, bf16 logits ~N(0,3); "
+            "per-request T in {0,0.5,1}, top_k in {0,20,50}, top_p in {1,0.9}, min_p in {0,0.05}; "
+            "Philox seed per request; point-mass draft")
+B, K, V = 128, 4, W.QWEN_VOCAB
+R = B * (K + 1)
+KERNEL_SOURCES = ["speculative_decoding_verification_ragged_gb300/csrc/verify.cu",
+                  "speculative_decoding_verification_ragged_gb300/csrc/common.cuh"]
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def traffic_record():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "verify_sample_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_sources_sha256_16") != kernel_digest():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------- clocks -----
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML (read-only) in a
+    background thread while the timed region runs."""
+    HW_SLOWDOWN, HW_THERMAL, SW_THERMAL, SW_POWER = 0x8, 0x40, 0x20, 0x4
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.samples, self.reasons = [], 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._period = period_s
+        self.ok = False
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self._period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self) -> dict:
+        names = []
+        for bit, n in [(self.HW_SLOWDOWN, "hw_slowdown"), (self.HW_THERMAL, "hw_thermal_slowdown"),
+                       (self.SW_THERMAL, "sw_thermal_slowdown"), (self.SW_POWER, "sw_power_cap")]:
+            if self.reasons & bit:
+                names.append(n)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples),
+                "source": "nvml" if self.ok else "unavailable"}
+
+
+# ------------------------------------------------------------ our arm -----
+
+def make_inputs(seed: int):
+    vb, p = W.stochastic(seed=seed)
+    return vb, p
+
+
+def run_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import speculative_decoding_verification_ragged_gb300 as sv
+    import speculative_decoding_verification_ragged_gb300.binding  # noqa: F401
+    sv.build()
+
+    vb, p = make_inputs(W.data_seed(3) + rank)
+    logits_host = torch.from_numpy(vb.logits.view(np.int16)).view(torch.bfloat16)
+    nsets = args.sets
+    sets = [logits_host.to(dev) for _ in range(nsets)]          # rotating copies > L2
+    cu = torch.from_numpy(vb.cu_rows).to(dev)
+    dr = torch.from_numpy(vb.draft_ids).to(dev)
+    tt = torch.from_numpy(p.temperature).to(dev)
+    tk = torch.from_numpy(p.top_k).to(dev)
+    tp = torch.from_numpy(p.top_p).to(dev)
+    mp = torch.from_numpy(p.min_p).to(dev)
+    sd = torch.from_numpy(p.seed.view(np.int64)).to(dev)
+    rid = torch.from_numpy(p.request_id.view(np.int32)).to(dev)
+    ws = sv.new_workspace(R, B, V, torch.bfloat16, dev, sampling=True)
+    acc = torch.zeros(K, dtype=torch.int64, device=dev)
+    ver = torch.zeros(K, dtype=torch.int64, device=dev)
+    hist = torch.zeros(K + 1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    call = sv.binding.PreparedSample(sets[0], cu, dr, tt, tk, tp, mp, sd, rid, V=V, B=B, k_max=K,
+                                     R_cap=R, workspace=ws, rows=True, stats=(acc, ver, hist),
+                                     stream=stream)
+
+    def step(i):
+        return call(sets[i % nsets], i)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    # per-launch events on the launching stream, plus the whole region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        torch.cuda._sleep(50_000_000)   # queue ahead of the device (outside the timed region)
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step(args.warmup + i)
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    mean_launch_ms = sum(launch_ms) / len(launch_ms)
+    if world > 1:
+        tt_ = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt_, op=dist.ReduceOp.MAX)
+        total_ms = float(tt_.item())
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory, the call, D2H of the step's results
+    pin = logits_host.pin_memory()
+    small_host = [torch.from_numpy(a).pin_memory() for a in
+                  [vb.cu_rows, vb.draft_ids, p.temperature, p.top_k, p.top_p, p.min_p,
+                   p.seed.view(np.int64), p.request_id.view(np.int32)]]
+    small_dev = [cu, dr, tt, tk, tp, mp, sd, rid]
+    out_host = {n: torch.empty(s, dtype=torch.int32).pin_memory()
+                for n, s in [("accepted_len", (B,)), ("out_tokens", (B, K + 1)),
+                             ("next_token", (B,))]}
+    h2d = pin.numel() * 2 + sum(x.numel() * x.element_size() for x in small_host)
+    d2h = sum(x.numel() * 4 for x in out_host.values())
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+
+    def e2e_step(i):
+        sets[0].copy_(pin, non_blocking=True)
+        for hsrc, ddst in zip(small_host, small_dev):
+            ddst.copy_(hsrc, non_blocking=True)
+        res = sv.verify_sample(sets[0], cu, dr, tt, tk, tp, mp, sd, rid, i, V=V, B=B, k_max=K,
+                               R_cap=R, workspace=ws, rows=False, stream=stream)
+        for n, h in out_host.items():
+            h.copy_(res[n], non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt_ = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt_, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt_.item())
+
+    entries = time_entry_points(sv, dev, stream, args) if (rank == 0 and not args.no_entries) else None
+
+    if rank == 0:
+        peaks = measured_peaks()
+        bytes_per_launch = (R * V * 2                      # logits, read once
+                            + (B + 1) * 4 + R * 4          # cu_rows, draft ids
+                            + B * (4 * 4 + 8 + 4)          # per-request parameters
+                            + B * 4 * (K + 3)              # request outputs
+                            + R * 4 * 4)                   # row outputs
+        achieved = bytes_per_launch / (mean_launch_ms * 1e-3) / 1e9
+        value = world * R * args.steps / (total_ms * 1e-3)
+        line = {
+            "metric": METRIC,
+            "value": round(value, 1),
+            "unit": "rows/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": B * world, "rows_per_step": R,
+                       "vocab": V, "draft_tokens": K, "parallelism": "replicas" if world > 1 else "1 gpu",
+                       "l2": "inputs rotate over %d device copies of %.1f MB each (> 129 MB L2)"
+                             % (nsets, R * V * 2 / 1e6)},
+            "hbm_gbs": round(achieved, 1),
+            "hbm_pct_of_peak": round(100 * achieved / peaks["hbm_gbs"], 1),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": traffic_record(), "peak_source": peaks["source"],
+                         "kernel": "verify_rows_kernel<bf16, sample>",
+                         "algorithmic_bytes_per_launch": bytes_per_launch,
+                         "mean_launch_us": round(mean_launch_ms * 1e3, 3)},
+            "e2e": {"value": round(world * R * e2e_steps / (e2e_ms * 1e-3), 1), "unit": "rows/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clocks.summary(),
+        }
+        if entries is not None:
+            for e in entries.values():
+                e["pct_of_peak"] = round(100 * e["hbm_gbs"] / peaks["hbm_gbs"], 1)
+            line["entry_points"] = entries
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(vb, p)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _time_launches(fn, n: int, stream) -> float:
+    """Mean device time (ms) of fn() over n launches, events on `stream`."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    torch.cuda._sleep(100_000_000)   # keep the GPU busy while the host queues the launches
+    for i in range(n):
+        ev[i][0].record(stream)
+        fn(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / n
+
+
+def time_entry_points(sv, dev, stream, args) -> dict:
+    """Device time of the other entry points at their workload shapes
+    (inputs rotate over device copies larger than L2)."""
+    import torch
+
+    def bf(x):
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    out = {}
+    n = args.entry_launches
+    # greedy verification, Qwen2.5-14B-shaped (B=128, k=4, V=152064, planted peaks)
+    vb = W.planted_greedy()
+    sets = [bf(vb.logits) for _ in range(args.sets)]
+    cu, dr = torch.from_numpy(vb.cu_rows).to(dev), torch.from_numpy(vb.draft_ids).to(dev)
+    ws = sv.new_workspace(vb.R, vb.B, vb.V, torch.bfloat16, dev)
+    fn = lambda i: sv.verify_greedy(sets[i % len(sets)], cu, dr, V=vb.V, B=vb.B, k_max=vb.k_max,
+                                    R_cap=vb.R, workspace=ws, rows=True, stream=stream)
+    for i in range(5):
+        fn(i)
+    ms = _time_launches(fn, n, stream)
+    out["spec_verify_greedy"] = {"workload": "B=128 k=4 V=152064 bf16 planted", "rows": vb.R,
+                                 "us": round(ms * 1e3, 2),
+                                 "hbm_gbs": round(vb.R * vb.V * 2 / (ms * 1e-3) / 1e9, 1)}
+    del sets
+    # relaxed top-K (EAGLE-relaxed, B=256, k=5, V=152064, K=4)
+    vb = W.relaxed_planted()
+    sets = [bf(vb.logits) for _ in range(2)]
+    cu, dr = torch.from_numpy(vb.cu_rows).to(dev), torch.from_numpy(vb.draft_ids).to(dev)
+    K = torch.from_numpy(vb.extra["relaxed_k"]).to(dev)
+    ws = sv.new_workspace(vb.R, vb.B, vb.V, torch.bfloat16, dev)
+    acc = torch.zeros(vb.k_max, dtype=torch.int64, device=dev)
+    ver, hist = acc.clone(), torch.zeros(vb.k_max + 1, dtype=torch.int64, device=dev)
+    fn = lambda i: sv.verify_relaxed_topk(sets[i % 2], cu, dr, K, V=vb.V, B=vb.B, k_max=vb.k_max,
+                                          R_cap=vb.R, workspace=ws, rows=True,
+                                          stats=(acc, ver, hist), stream=stream)
+    for i in range(5):
+        fn(i)
+    ms = _time_launches(fn, n, stream)
+    out["spec_verify_relaxed_topk"] = {"workload": "B=256 k=5 V=152064 bf16 K=4 + fused stats",
+                                       "rows": vb.R, "us": round(ms * 1e3, 2),
+                                       "hbm_gbs": round(vb.R * vb.V * 2 / (ms * 1e-3) / 1e9, 1)}
+    del sets
+    # draft confidence + allocation (MTP/DSpark-shaped, B=16, k=7, V=151552)
+    db = W.mtp_adaptive(planted_draft=True)
+    dsets = [bf(db.draft_logits) for _ in range(8)]
+    dws = sv.binding.new_draft_workspace(db.B, db.k, db.V, torch.bfloat16, dev)
+    fn = lambda i: sv.draft_confidence(dsets[i % 8], V=db.V, B=db.B, k=db.k, threshold=0.3,
+                                       workspace=dws, stream=stream)
+    for i in range(5):
+        fn(i)
+    ms = _time_launches(fn, n, stream)
+    rows = db.B * db.k
+    out["spec_draft_confidence"] = {"workload": "B=16 k=7 V=151552 bf16, threshold 0.3",
+                                    "rows": rows, "us": round(ms * 1e3, 2),
+                                    "hbm_gbs": round(rows * db.V * 2 / (ms * 1e-3) / 1e9, 1)}
+    # standalone prefix statistics
+    a = torch.randint(0, 5, (128,), dtype=torch.int32, device=dev)
+    cu = torch.arange(0, 129 * 5, 5, dtype=torch.int32, device=dev)
+    acc = torch.zeros(4, dtype=torch.int64, device=dev)
+    ver, hist = acc.clone(), torch.zeros(5, dtype=torch.int64, device=dev)
+    fn = lambda i: sv.prefix_stats(a, cu, acc, ver, hist, B=128, k_max=4, stream=stream)
+    ms = _time_launches(fn, n, stream)
+    out["spec_prefix_stats"] = {"workload": "B=128 k=4", "us": round(ms * 1e3, 2), "hbm_gbs": 0.0}
+    return out
+
+
+def cpu_baseline(vb, p, budget_s: float = 10.0) -> dict:
+    """The oracle as it stands, on the host cores, over whole batches of the
+    same workload, repeated until about budget_s of CPU time has passed."""
+    import oracle
+    oracle.build()
+    cores = oracle.threads(len(os.sched_getaffinity(0)))
+    rows = 0
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.verify_sample(vb.logits, vb.dtype, vb.V, vb.B, vb.k_max, vb.cu_rows, vb.draft_ids, p)
+        rows += vb.R
+        n += 1
+        if time.perf_counter() - t0 > budget_s or n >= 20:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(rows / dt, 2), "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": "%d full batch(es) of the benchmark workload (%d rows each), fp64 C oracle "
+                      "with OpenMP over rows" % (n, vb.R)}
+
+
+# ------------------------------------------------------ reference arm -----
+
+def run_reference(args) -> None:
+    """The CPU oracle timed on the host cores on this workload: each step is
+    one packed row of the batch (cycling), sampled exactly as defined."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cores = oracle.threads(1)
+    vb, p = make_inputs(W.data_seed(3))
+    vals = W.bf16_bits_to_f32(vb.logits).astype(np.float64)
+    owner = np.repeat(np.arange(B), K + 1)
+
+    def step(i):
+        r = i % R
+        b = int(owner[r])
+        oracle.sample_row(vals[r, :V], float(p.temperature[b]), int(p.top_k[b]), float(p.top_p[b]),
+                          float(p.min_p[b]), int(p.seed[b]), int(p.request_id[b]), r - b * (K + 1),
+                          p.step)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "rows/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "global_batch": B,
+                                        "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "rows/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": "one packed row of the benchmark batch per step (cycling)"},
+        "e2e": {"value": round(value, 3), "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sets", type=int, default=4, help="rotating device copies of the inputs")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-entries", action="store_true", help="skip the other entry points")
+    ap.add_argument("--entry-launches", type=int, default=50)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,15 @@
+"""GB300-native batched draft-token verification for speculative decoding.
+
+The compute path is libspecverify.so (hand-written sm_103a CUDA behind the C
+ABI in include/spec_verify.h); this package holds its sources (csrc/), the
+in-tree build (_build.py) and a thin ctypes binding (binding.py).
+"""
+from ._build import build  # noqa: F401
+from .binding import (  # noqa: F401
+    EXPORTS, SpecError, draft_confidence, load_library, new_workspace, prefix_stats,
+    verify_greedy, verify_relaxed_topk, verify_sample, workspace_bytes,
+)
+
+__all__ = ["build", "load_library", "new_workspace", "workspace_bytes", "verify_greedy",
+           "verify_relaxed_topk", "verify_sample", "draft_confidence", "prefix_stats",
+           "SpecError", "EXPORTS"]

@@ -1,0 +1,345 @@
+"""Thin ctypes binding of libspecverify (include/spec_verify.h).
+
+Argument marshalling only: every step of verification runs in the CUDA
+kernels of libspecverify.so.  PyTorch supplies device memory and the current
+stream.  There is no CPU fallback: if the library is missing or no CUDA
+device is present, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+_LIB_PATH = _build.OUT
+
+SPEC_F32, SPEC_BF16 = 0, 1
+RESULT_NAMES = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_UNSUPPORTED",
+                3: "SPEC_ERR_CUDA", 4: "SPEC_ERR_WORKSPACE"}
+
+STATUS_BAD_TEMPERATURE = 0x1
+STATUS_BAD_TOP_K = 0x2
+STATUS_BAD_TOP_P = 0x4
+STATUS_BAD_MIN_P = 0x8
+STATUS_BAD_ROWS = 0x10
+STATUS_BAD_SELECTED = 0x20
+STATUS_BAD_RELAXED_K = 0x40
+STATUS_BAD_BUDGET = 0x80
+STATUS_TIMEOUT = 0x100
+
+EXPORTS = ["spec_workspace_bytes", "spec_draft_workspace_bytes", "spec_verify_greedy", "spec_verify_relaxed_topk",
+           "spec_verify_sample", "spec_draft_confidence", "spec_prefix_stats",
+           "spec_result_string", "spec_last_cuda_error", "spec_abi_version"]
+
+
+class SpecError(RuntimeError):
+    pass
+
+
+class Batch(C.Structure):
+    _fields_ = [("logits", C.c_void_p), ("dtype", C.c_int32), ("V", C.c_int32),
+                ("ld", C.c_int64), ("B", C.c_int32), ("k_max", C.c_int32),
+                ("R_cap", C.c_int32), ("cu_rows", C.c_void_p), ("draft_ids", C.c_void_p)]
+
+
+class Outputs(C.Structure):
+    _fields_ = [("accepted_len", C.c_void_p), ("out_tokens", C.c_void_p),
+                ("next_token", C.c_void_p), ("row_max", C.c_void_p), ("row_lse", C.c_void_p),
+                ("row_argmax", C.c_void_p), ("row_token", C.c_void_p), ("status", C.c_void_p),
+                ("acc", C.c_void_p), ("ver", C.c_void_p), ("hist", C.c_void_p)]
+
+
+class Sampling(C.Structure):
+    _fields_ = [("temperature", C.c_void_p), ("top_k", C.c_void_p), ("top_p", C.c_void_p),
+                ("min_p", C.c_void_p), ("seed", C.c_void_p), ("request_id", C.c_void_p),
+                ("step", C.c_uint32)]
+
+
+class Draft(C.Structure):
+    _fields_ = [("draft_logits", C.c_void_p), ("dtype", C.c_int32), ("V", C.c_int32),
+                ("ld", C.c_int64), ("B", C.c_int32), ("k", C.c_int32),
+                ("selected", C.c_void_p), ("threshold", C.c_float), ("max_rows", C.c_int32)]
+
+
+class Allocation(C.Structure):
+    _fields_ = [("conf", C.c_void_p), ("draft_token", C.c_void_p), ("k_alloc", C.c_void_p),
+                ("cu_rows", C.c_void_p), ("row_owner", C.c_void_p), ("row_pos", C.c_void_p),
+                ("packed_draft", C.c_void_p), ("total_rows", C.c_void_p),
+                ("status", C.c_void_p)]
+
+
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> C.CDLL:
+    """Load libspecverify.so (no device needed).  Raises if it was not built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise SpecError("libspecverify.so is not built (%s); run the package build first" % p)
+    L = C.CDLL(p)
+    vp, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
+    L.spec_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    L.spec_draft_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.spec_draft_workspace_bytes.restype = C.c_size_t
+    L.spec_workspace_bytes.restype = C.c_size_t
+    L.spec_verify_greedy.argtypes = [C.POINTER(Batch), C.POINTER(Outputs), vp, C.c_size_t, vp]
+    L.spec_verify_relaxed_topk.argtypes = [C.POINTER(Batch), vp, C.POINTER(Outputs), vp,
+                                           C.c_size_t, vp]
+    L.spec_verify_sample.argtypes = [C.POINTER(Batch), C.POINTER(Sampling), C.POINTER(Outputs),
+                                     vp, C.c_size_t, vp]
+    L.spec_draft_confidence.argtypes = [C.POINTER(Draft), C.POINTER(Allocation), vp, C.c_size_t,
+                                        vp]
+    L.spec_prefix_stats.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp]
+    for f in ["spec_verify_greedy", "spec_verify_relaxed_topk", "spec_verify_sample",
+              "spec_draft_confidence", "spec_prefix_stats", "spec_abi_version"]:
+        getattr(L, f).restype = C.c_int
+    L.spec_result_string.argtypes = [C.c_int]
+    L.spec_result_string.restype = C.c_char_p
+    L.spec_last_cuda_error.restype = C.c_char_p
+    if path is None:
+        _lib = L
+    return L
+
+
+def _check(rc: int):
+    if rc != 0:
+        L = load_library()
+        msg = RESULT_NAMES.get(rc, str(rc))
+        if rc == 3:
+            msg += ": " + L.spec_last_cuda_error().decode()
+        raise SpecError(msg)
+
+
+def _dev(t: Optional[torch.Tensor], what: str, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise SpecError("%s must be a CUDA tensor" % what)
+    if dtype is not None and t.dtype != dtype:
+        raise SpecError("%s must have dtype %s, got %s" % (what, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise SpecError("%s must be contiguous" % what)
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _logits_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16 or t.dtype == torch.int16 or t.dtype == torch.uint16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise SpecError("logits must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def workspace_bytes(R_cap: int, B: int, V: int, dtype=SPEC_BF16, sampling: bool = False) -> int:
+    return int(load_library().spec_workspace_bytes(int(R_cap), int(B), int(V), int(dtype),
+                                                   int(bool(sampling))))
+
+
+def _dtype_code(dtype) -> int:
+    if isinstance(dtype, int):
+        return dtype
+    return SPEC_F32 if dtype in (torch.float32, "f32") else SPEC_BF16
+
+
+def new_workspace(R_cap: int, B: int, V: int, dtype=SPEC_BF16, device=None,
+                  sampling: bool = False) -> torch.Tensor:
+    """Zero-filled workspace for the verify calls (reusable, stream-ordered);
+    sampling=True sizes it for spec_verify_sample."""
+    n = workspace_bytes(R_cap, B, V, _dtype_code(dtype), sampling)
+    if n == 0:
+        raise SpecError("invalid workspace size for R_cap=%d B=%d V=%d" % (R_cap, B, V))
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def new_draft_workspace(B: int, k: int, V: int, dtype=SPEC_BF16, device=None) -> torch.Tensor:
+    n = int(load_library().spec_draft_workspace_bytes(int(B), int(k), int(V), _dtype_code(dtype)))
+    if n == 0:
+        raise SpecError("invalid draft workspace size")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids) -> Batch:
+    if logits.dim() != 2:
+        raise SpecError("logits must be 2-D [rows, ld]")
+    if logits.stride(1) != 1:
+        raise SpecError("logits rows must be contiguous")
+    return Batch(_dev(logits, "logits"), _logits_dtype(logits), int(V), int(logits.stride(0)),
+                 int(B), int(k_max), int(R_cap), _dev(cu_rows, "cu_rows", torch.int32),
+                 _dev(draft_ids, "draft_ids", torch.int32))
+
+
+def _outputs(B, k_max, R_cap, device, rows: bool, stats) -> tuple:
+    res = {
+        "accepted_len": torch.empty(B, dtype=torch.int32, device=device),
+        "out_tokens": torch.empty(B, k_max + 1, dtype=torch.int32, device=device),
+        "next_token": torch.empty(B, dtype=torch.int32, device=device),
+        "status": torch.zeros(1, dtype=torch.int32, device=device),
+    }
+    if rows:
+        res["row_max"] = torch.empty(R_cap, dtype=torch.float32, device=device)
+        res["row_lse"] = torch.empty(R_cap, dtype=torch.float32, device=device)
+        res["row_argmax"] = torch.empty(R_cap, dtype=torch.int32, device=device)
+        res["row_token"] = torch.empty(R_cap, dtype=torch.int32, device=device)
+    o = Outputs(res["accepted_len"].data_ptr(), res["out_tokens"].data_ptr(),
+                res["next_token"].data_ptr(),
+                res["row_max"].data_ptr() if rows else None,
+                res["row_lse"].data_ptr() if rows else None,
+                res["row_argmax"].data_ptr() if rows else None,
+                res["row_token"].data_ptr() if rows else None,
+                res["status"].data_ptr(), None, None, None)
+    if stats is not None:
+        acc, ver, hist = stats
+        o.acc = _dev(acc, "acc", torch.int64)
+        o.ver = _dev(ver, "ver", torch.int64)
+        o.hist = _dev(hist, "hist", torch.int64)
+    return o, res
+
+
+def verify_greedy(logits, cu_rows, draft_ids, *, V: int, B: int, k_max: int,
+                  R_cap: Optional[int] = None, workspace=None, rows: bool = True, stats=None,
+                  stream=None) -> dict:
+    """spec_verify_greedy: fused max/LSE/argmax per row, then greedy prefix
+    acceptance per request.  Returns a dict of device tensors."""
+    L = load_library()
+    R_cap = R_cap or B * (k_max + 1)
+    ws = workspace if workspace is not None else new_workspace(
+        R_cap, B, V, _logits_dtype(logits), logits.device)
+    b = _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids)
+    o, res = _outputs(B, k_max, R_cap, logits.device, rows, stats)
+    _check(L.spec_verify_greedy(C.byref(b), C.byref(o), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return res
+
+
+def verify_relaxed_topk(logits, cu_rows, draft_ids, relaxed_k, *, V: int, B: int, k_max: int,
+                        R_cap: Optional[int] = None, workspace=None, rows: bool = True,
+                        stats=None, stream=None) -> dict:
+    """spec_verify_relaxed_topk: accept d iff #{z > z_d} < K_b, strict prefix."""
+    L = load_library()
+    R_cap = R_cap or B * (k_max + 1)
+    ws = workspace if workspace is not None else new_workspace(
+        R_cap, B, V, _logits_dtype(logits), logits.device)
+    b = _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids)
+    o, res = _outputs(B, k_max, R_cap, logits.device, rows, stats)
+    _check(L.spec_verify_relaxed_topk(C.byref(b), _dev(relaxed_k, "relaxed_k", torch.int32),
+                                      C.byref(o), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return res
+
+
+def verify_sample(logits, cu_rows, draft_ids, temperature, top_k, top_p, min_p, seed,
+                  request_id=None, step: int = 0, *, V: int, B: int, k_max: int,
+                  R_cap: Optional[int] = None, workspace=None, rows: bool = True, stats=None,
+                  stream=None) -> dict:
+    """spec_verify_sample: filtered Gumbel-max sampling per row (Philox4x32-10
+    uniforms) and the point-mass rejection chain per request.  `seed` is an
+    int64 tensor holding the 64-bit seeds' bit patterns."""
+    L = load_library()
+    R_cap = R_cap or B * (k_max + 1)
+    ws = workspace if workspace is not None else new_workspace(
+        R_cap, B, V, _logits_dtype(logits), logits.device, sampling=True)
+    b = _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids)
+    s = Sampling(_dev(temperature, "temperature", torch.float32), _dev(top_k, "top_k", torch.int32),
+                 _dev(top_p, "top_p", torch.float32), _dev(min_p, "min_p", torch.float32),
+                 _dev(seed, "seed", torch.int64),
+                 _dev(request_id, "request_id", torch.int32) if request_id is not None else None,
+                 int(step) & 0xFFFFFFFF)
+    o, res = _outputs(B, k_max, R_cap, logits.device, rows, stats)
+    _check(L.spec_verify_sample(C.byref(b), C.byref(s), C.byref(o), ws.data_ptr(), ws.numel(),
+                                _stream(stream)))
+    return res
+
+
+def draft_confidence(draft_logits, *, V: int, B: int, k: int, selected=None,
+                     threshold: float = 0.3, max_rows: int = 0, workspace=None,
+                     stream=None) -> dict:
+    """spec_draft_confidence: conf = exp(z[s] - logsumexp(z)) per draft row,
+    then device-side prefix allocation and packing."""
+    L = load_library()
+    dev = draft_logits.device
+    if draft_logits.dim() != 2 or draft_logits.stride(1) != 1:
+        raise SpecError("draft_logits must be 2-D with contiguous rows")
+    d = Draft(_dev(draft_logits, "draft_logits"), _logits_dtype(draft_logits), int(V),
+              int(draft_logits.stride(0)), int(B), int(k),
+              _dev(selected, "selected", torch.int32) if selected is not None else None,
+              float(threshold), int(max_rows))
+    cap = B * (k + 1)
+    res = {
+        "conf": torch.empty(B * k, dtype=torch.float32, device=dev),
+        "draft_token": torch.empty(B * k, dtype=torch.int32, device=dev),
+        "k_alloc": torch.empty(B, dtype=torch.int32, device=dev),
+        "cu_rows": torch.empty(B + 1, dtype=torch.int32, device=dev),
+        "row_owner": torch.empty(cap, dtype=torch.int32, device=dev),
+        "row_pos": torch.empty(cap, dtype=torch.int32, device=dev),
+        "packed_draft": torch.empty(cap, dtype=torch.int32, device=dev),
+        "total_rows": torch.empty(1, dtype=torch.int32, device=dev),
+        "status": torch.zeros(1, dtype=torch.int32, device=dev),
+    }
+    a = Allocation(*[res[n].data_ptr() for n in ["conf", "draft_token", "k_alloc", "cu_rows",
+                                                  "row_owner", "row_pos", "packed_draft",
+                                                  "total_rows", "status"]])
+    ws = workspace if workspace is not None else new_draft_workspace(
+        B, k, V, _logits_dtype(draft_logits), dev)
+    _check(L.spec_draft_confidence(C.byref(d), C.byref(a), ws.data_ptr(), ws.numel(),
+                                   _stream(stream)))
+    return res
+
+
+def prefix_stats(accepted_len, cu_rows, acc, ver, hist=None, status=None, *, B: int, k_max: int,
+                 stream=None):
+    """spec_prefix_stats: accumulate per-position prefix-acceptance counters
+    (int64 tensors acc[k_max], ver[k_max], hist[k_max+1]) in place."""
+    L = load_library()
+    _check(L.spec_prefix_stats(_dev(accepted_len, "accepted_len", torch.int32),
+                               _dev(cu_rows, "cu_rows", torch.int32), int(B), int(k_max),
+                               _dev(acc, "acc", torch.int64), _dev(ver, "ver", torch.int64),
+                               _dev(hist, "hist", torch.int64) if hist is not None else None,
+                               _dev(status, "status", torch.int32) if status is not None else None,
+                               _stream(stream)))
+
+
+class PreparedSample:
+    """A spec_verify_sample call with every argument marshalled once; each
+    __call__ swaps only the logits pointer and the step word, so a loop of
+    calls costs one ctypes call per launch (for benchmarking and serving
+    loops).  The tensors passed here must stay alive while it is used."""
+
+    def __init__(self, logits, cu_rows, draft_ids, temperature, top_k, top_p, min_p, seed,
+                 request_id=None, *, V: int, B: int, k_max: int, R_cap: Optional[int] = None,
+                 workspace=None, rows: bool = True, stats=None, stream=None):
+        self.L = load_library()
+        R_cap = R_cap or B * (k_max + 1)
+        self.ws = workspace if workspace is not None else new_workspace(
+            R_cap, B, V, _logits_dtype(logits), logits.device, sampling=True)
+        self.batch = _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids)
+        self.samp = Sampling(_dev(temperature, "temperature", torch.float32),
+                             _dev(top_k, "top_k", torch.int32), _dev(top_p, "top_p", torch.float32),
+                             _dev(min_p, "min_p", torch.float32), _dev(seed, "seed", torch.int64),
+                             _dev(request_id, "request_id", torch.int32)
+                             if request_id is not None else None, 0)
+        self.out, self.res = _outputs(B, k_max, R_cap, logits.device, rows, stats)
+        self.stream = _stream(stream)
+        self._keep = (logits, cu_rows, draft_ids, temperature, top_k, top_p, min_p, seed,
+                      request_id, stats)
+        self._args = (C.byref(self.batch), C.byref(self.samp), C.byref(self.out),
+                      C.c_void_p(self.ws.data_ptr()), C.c_size_t(self.ws.numel()),
+                      C.c_void_p(self.stream))
+
+    def __call__(self, logits=None, step: int = 0) -> dict:
+        if logits is not None:
+            self.batch.logits = logits.data_ptr()
+        self.samp.step = int(step) & 0xFFFFFFFF
+        rc = self.L.spec_verify_sample(*self._args)
+        if rc:
+            _check(rc)
+        return self.res

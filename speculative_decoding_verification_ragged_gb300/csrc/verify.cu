@@ -1,0 +1,1118 @@
+// verify.cu -- kernels for ragged packed logits: fused max / LSE / argmax,
+// greedy and relaxed top-K acceptance, the filtered Gumbel-max sampler with
+// the point-mass rejection chain, and the draft confidence.
+//
+// Three kernels per call, chained with programmatic dependent launch:
+//
+//   prologue, one warp per packed row: the owner request (32-way search of
+//     cu_rows), the row's position and validity and the owner's parameters,
+//     as a 64-byte row record; requests without a valid row range get their
+//     outputs here.
+//   stream, one CTA per (row, chunk of kChunkBytes): thread 0 stages the
+//     chunk's 16-byte-aligned body in shared memory with one 1-D TMA bulk
+//     copy and the row record with a second, on one mbarrier (the row is read
+//     from HBM exactly once; unaligned head/tail elements use plain loads).
+//     Pass 1 runs a per-thread online max / first argmax / sum exp(z - max)
+//     over 16-byte vectors (packed bf16x2 max per vector; two independent
+//     accumulators), plus the count of logits above the draft's logit for
+//     relaxed top-K; warp shuffles and a CTA reduction give the chunk
+//     summary.  For the sampler (T > 0) the survivors form an upper set
+//     {z >= th}: with top-k or min-p the chunk bounds th from below (chunk max
+//     + T ln min_p; a ladder level below the chunk max holding k thread
+//     maxima) and stores the elements above the bound as candidates; with no
+//     filter it stores its own Gumbel-max winner; with pure top-p it stores
+//     its mass exp((z - m_c)/T) in bins of T/8 below its maximum.  Only plain
+//     stores: nothing in this kernel waits for, or fences against, another
+//     CTA.
+//   finish, one CTA per row: combine the chunk summaries in parallel, then
+//     for the sampler run 8-bit radix selects (exact k-th largest value,
+//     exact top-p mass crossing) over the candidates and Gumbel-max over the
+//     survivors with Philox4x32-10 uniforms.  Pure top-p brackets the nucleus
+//     boundary with the chunk bins and settles it exactly on the one band of
+//     values the bins cannot decide, from a single pass over the row (L2)
+//     streamed through shared memory by TMA.  The CTA finishing the last row
+//     of a request (atomic ticket) runs the accept-while-equal prefix scan
+//     with one warp ballot and writes the request's tokens and the optional
+//     prefix-acceptance counters.
+//
+// Definitions: xLLM docs "自适应投机推理" §"启动示例" (ragged rejection
+// sampler with packed-row owners, point-mass draft, replacement / bonus,
+// temperature 0 = greedy, ordinary top-k/top-p/min-p semantics),
+// §"基于 MTP logits 的自适应 target 验证" (exp(selected - logsumexp)),
+// "vllm-hust-vSpec" README §"EAGLE 功能" (strict top-1 and relaxed top-K
+// acceptance with a strict prefix, no per-request host sync).
+#include <cfloat>
+#include <climits>
+#include <cmath>
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace specv {
+
+constexpr int kCandCap = kWsCandCap;    // candidates one chunk may store
+constexpr int kBins = kWsBins;          // pure top-p mass bins per chunk
+constexpr float kBinsPerT = 8.0f;       // bin width T/8
+constexpr int kBandCap = 4096;          // undecided values the finish kernel keeps on chip
+constexpr int kRowStage = 16 * 1024;    // finish kernel: bytes per row-streaming stage
+
+// row record written by the prologue (64 bytes)
+struct __align__(16) RowInfo {
+    int32_t b, pos, k_b, valid;
+    int32_t draft, K, top_k, bad;
+    float T, top_p, min_p, zd;
+    uint32_t seed_lo, seed_hi, rid, sel;
+};
+static_assert(sizeof(RowInfo) == 64, "row record is 64 bytes");
+
+// chunk summary kept in the workspace (32 bytes)
+struct __align__(16) ChunkPart {
+    float m;        // chunk max
+    int32_t amax;   // first argmax in the chunk
+    float s;        // sum exp(z - m)
+    int32_t cnt;    // relaxed: logits above the draft's
+    float gbest;    // sampler, no filter: best Gumbel score; pure top-p: mass sum
+    int32_t gidx;   //   and its index
+    int32_t ncand;  // sampler with a bound: candidates (> kCandCap: overflow)
+    int32_t pad;
+};
+
+// shared scratch common to both row kernels
+struct __align__(16) Shared {
+    RowInfo info;
+    ChunkPart part;
+    uint32_t hist[256];
+    uint32_t scan[kWarps];
+    float red_f[kWarps * 2];
+    int32_t red_i[kWarps * 2];
+    float M, S, W, sel_t, sel_excl_f, excl_band;
+    int32_t AMAX, CNT, sel_bin, sel_found, total, overflow, cand_n, R, band_lo, band_hi;
+    uint32_t sel_excl_u;
+    float extras_v[16];
+    int32_t extras_i[16];
+    int32_t timeout;
+    uint64_t mbar[2];
+};
+
+struct Cand {
+    float v;
+    int32_t i;
+};
+
+// ------------------------------------------------------------ helpers -----
+
+// combine two (max, first-argmax, scaled sum, count) partials
+__device__ __forceinline__ void combine(float &m, int32_t &a, float &s, int32_t &c, float om,
+                                        int32_t oa, float os, int32_t oc, bool need_sum)
+{
+    const float nm = fmaxf(m, om);
+    if (need_sum) {
+        const float s1 = (m > -INFINITY) ? s * ex2((m - nm) * kLog2e) : 0.f;
+        const float s2 = (om > -INFINITY) ? os * ex2((om - nm) * kLog2e) : 0.f;
+        s = s1 + s2;
+    }
+    if (om > m || (om == m && oa < a)) a = oa;
+    m = nm;
+    c += oc;
+}
+
+// Block-wide search, from the top bin (255) down, of the bin where the running
+// total first reaches `target` (thread t holds bin 255 - t).  Writes
+// sh.sel_bin and the total above that bin; when rounding keeps the float
+// total below the target, the lowest non-empty bin is taken.
+template <typename V>
+__device__ void find_crossing(const V *hist, V target, Shared &sh)
+{
+    constexpr bool IS_F = std::is_same<V, float>::value;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const V v = hist[255 - t];
+    V incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const V n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    V *wt = reinterpret_cast<V *>(sh.scan);
+    if (lane == 31) wt[warp] = incl;
+    if (t == 0) sh.sel_found = 0;
+    __syncthreads();
+    V off = V(0);
+    for (int w = 0; w < warp; ++w) off += wt[w];
+    incl += off;
+    const V excl = incl - v;
+    if (v > V(0) && excl < target && target <= incl) {
+        sh.sel_found = 1;
+        sh.sel_bin = 255 - t;
+        if constexpr (IS_F) sh.sel_excl_f = excl;
+        else sh.sel_excl_u = excl;
+    }
+    __syncthreads();
+    if (!sh.sel_found) {
+        if (t == 0) {
+            int best = -1;
+            V run = V(0), before = V(0);
+            for (int q = 255; q >= 0; --q)
+                if (hist[q] > V(0)) { best = q; before = run; run += hist[q]; }
+            sh.sel_bin = best;
+            if constexpr (IS_F) sh.sel_excl_f = before;
+            else sh.sel_excl_u = before;
+        }
+        __syncthreads();
+    }
+}
+
+// final 32-bit key from the 8-bit digits chosen (bf16 keys use bits 31..16)
+__device__ __forceinline__ uint32_t finish_key(uint32_t prefix, int passes)
+{
+    if (passes == 2) return (prefix << 16) | ((prefix & 0x8000u) ? 0u : 0xFFFFu);
+    return prefix;
+}
+
+// Float threshold equivalent to "key >= k": -inf for the keys below -inf's.
+__device__ __forceinline__ float key_floor(uint32_t k)
+{
+    return (k <= 0x007FFFFFu) ? -INFINITY : key_value(k);
+}
+
+// CTA-local radix select over the values produced by `visit(fn, thr)` (fn(v,
+// i) for every element >= thr): the key of the k-th largest value, or of the
+// value group where the cumulative weight exp((z - M) * sc) counted from the
+// top first reaches `target`.  Only values with key >= key_min take part.
+template <bool MASS, typename Visit>
+__device__ uint32_t radix_select(Visit &&visit, uint32_t key_min, float target, uint32_t k,
+                                 float M, float sc, int passes, Shared &sh)
+{
+    uint32_t prefix = 0;
+    const float thr = key_floor(key_min);
+    for (int pass = 0; pass < passes; ++pass) {
+        const int shift = 24 - 8 * pass;
+        sh.hist[threadIdx.x] = 0u;
+        __syncthreads();
+        visit([&](float v, int32_t) {
+            const uint32_t key = fkey(v);
+            if (key < key_min) return;
+            if (pass > 0 && (key >> (shift + 8)) != prefix) return;
+            const uint32_t bin = (key >> shift) & 255u;
+            if (MASS) atomicAdd(reinterpret_cast<float *>(&sh.hist[bin]), ex2((v - M) * sc));
+            else atomicAdd(&sh.hist[bin], 1u);
+        }, thr);
+        __syncthreads();
+        if (MASS) find_crossing<float>(reinterpret_cast<const float *>(sh.hist), target, sh);
+        else find_crossing<uint32_t>(sh.hist, k, sh);
+        const int bin = sh.sel_bin;
+        if (MASS) target -= sh.sel_excl_f;
+        else k -= sh.sel_excl_u;
+        prefix = (prefix << 8) | static_cast<uint32_t>(bin < 0 ? 0 : bin);
+        __syncthreads();
+    }
+    return finish_key(prefix, passes);
+}
+
+// block reduction of a float sum (result in every thread)
+__device__ __forceinline__ float block_sum(float v, Shared &sh)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if ((threadIdx.x & 31) == 0) sh.red_f[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int q = 0; q < kWarps; ++q) t += sh.red_f[q];
+    __syncthreads();
+    return t;
+}
+
+// block reduction of a (score, index) maximum, lowest index on ties
+__device__ __forceinline__ void block_best(float &best, int32_t &bi, Shared &sh)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        const int32_t oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+        if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+    }
+    if ((threadIdx.x & 31) == 0) { sh.red_f[threadIdx.x >> 5] = best; sh.red_i[threadIdx.x >> 5] = bi; }
+    __syncthreads();
+    best = -INFINITY;
+    bi = INT_MAX;
+    for (int q = 0; q < kWarps; ++q)
+        if (sh.red_f[q] > best || (sh.red_f[q] == best && sh.red_i[q] < bi)) { best = sh.red_f[q]; bi = sh.red_i[q]; }
+    __syncthreads();
+}
+
+// Top-k bound inside a chunk: the highest level L = m_c - D (D from a fixed
+// ladder) with at least k thread maxima >= L.  Thread maxima are distinct
+// elements, so at least k elements of the chunk are >= L and the chunk's
+// share of the row's top k lies above it.  False if no level qualifies.
+__device__ __forceinline__ bool kth_level(float thread_max, float m_c, int k, float &level,
+                                          Shared &sh)
+{
+    constexpr int NL = 8;
+    const float ladder[NL] = {0.25f, 0.5f, 1.f, 2.f, 3.f, 4.f, 6.f, 8.f};
+    int cnt[NL];
+#pragma unroll
+    for (int l = 0; l < NL; ++l) cnt[l] = (thread_max >= m_c - ladder[l]) ? 1 : 0;
+#pragma unroll
+    for (int l = 0; l < NL; ++l) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt[l] += __shfl_xor_sync(0xFFFFFFFFu, cnt[l], o);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int *wc = reinterpret_cast<int *>(sh.hist);        // [kWarps][NL]
+    if (lane == 0)
+#pragma unroll
+        for (int l = 0; l < NL; ++l) wc[warp * NL + l] = cnt[l];
+    __syncthreads();
+    int sel = -1;
+    for (int l = 0; l < NL; ++l) {
+        int t = 0;
+        for (int w = 0; w < kWarps; ++w) t += wc[w * NL + l];
+        if (t >= k) { sel = l; break; }
+    }
+    __syncthreads();
+    if (sel < 0) return false;
+    level = m_c - ladder[sel];
+    return true;
+}
+
+// Gumbel-perturbed score z/T - log(-log u_i), u_i from Philox4x32-10 with
+// counter (i >> 2, position, request id, step) and key (seed lo, seed hi).
+struct GumbelScorer {
+    float invT;
+    uint32_t pos, rid, step, k0, k1;
+    uint32_t cached;
+    uint4 words;
+    __device__ __forceinline__ float operator()(float v, int32_t ix)
+    {
+        const uint32_t ctr = static_cast<uint32_t>(ix) >> 2;
+        if (ctr != cached) {
+            words = philox4x32_10(make_uint4(ctr, pos, rid, step), k0, k1);
+            cached = ctr;
+        }
+        return fmaf(v, invT, gumbel_of(word_of(words, static_cast<uint32_t>(ix) & 3u)));
+    }
+};
+
+// Pass 1 over this thread's 16-byte vectors of the staged chunk: running max
+// with the first index attaining it, and (SUM) sum exp(z - running max)
+// rescaled when the max grows.  The running max starts at a finite sentinel
+// far below any logit, so -inf logits contribute exp(-inf) = 0 without a
+// per-vector test; a chunk of only -inf reports -inf.
+constexpr float kSentinel = -1.0e38f;
+
+template <typename E, int MODE, bool SUM>
+__device__ __forceinline__ float pass1(const uint4 *body, int nb, int a0, float zd, int32_t &targ,
+                                       float &tsum, int32_t &tcnt)
+{
+    constexpr int VEC = E::VEC;
+    float tmax = kSentinel;
+    float s0 = 0.f, s1 = 0.f;     // two accumulators: independent add chains
+    for (int i = threadIdx.x; i < nb; i += kThreads) {
+        const uint4 v = body[i];
+        const float vm = E::vmax(v);
+        float x[VEC];
+        E::unpack(v, x);
+        if (vm > tmax) {
+            int first = VEC - 1;
+#pragma unroll
+            for (int j = VEC - 1; j >= 0; --j)
+                if (x[j] == vm) first = j;
+            if (SUM) {
+                const float f = ex2((tmax - vm) * kLog2e);
+                s0 *= f;
+                s1 *= f;
+            }
+            tmax = vm;
+            targ = a0 + i * VEC + first;
+        }
+        if (SUM) {
+            const float c0 = -tmax * kLog2e;
+#pragma unroll
+            for (int j = 0; j < VEC; j += 2) {
+                s0 += ex2(fmaf(x[j], kLog2e, c0));
+                s1 += ex2(fmaf(x[j + 1], kLog2e, c0));
+            }
+        }
+        if (MODE == MODE_RELAXED) {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) tcnt += (x[j] > zd) ? 1 : 0;
+        }
+    }
+    tsum = s0 + s1;
+    if (tmax == kSentinel) { tmax = -INFINITY; tsum = 0.f; }
+    return tmax;
+}
+
+template <typename E, int MODE>
+__device__ __forceinline__ float pass1_sum(const uint4 *body, int nb, int a0, float zd,
+                                           int32_t &targ, float &tsum, int32_t &tcnt)
+{
+    return pass1<E, MODE, true>(body, nb, a0, zd, targ, tsum, tcnt);
+}
+
+template <typename E, int MODE>
+__device__ __forceinline__ float pass1_nosum(const uint4 *body, int nb, int a0, float zd,
+                                             int32_t &targ, float &tsum, int32_t &tcnt)
+{
+    return pass1<E, MODE, false>(body, nb, a0, zd, targ, tsum, tcnt);
+}
+
+// chunk c of a row: elements [e0, e1); 16-byte-aligned body of nb vectors
+// from element a0; head [e0, a0) and tail [a1, e1) use plain loads
+struct ChunkGeom {
+    int e0, e1, a0, nb, a1, n_head, n_extra, h;
+};
+
+template <typename E>
+__device__ __forceinline__ ChunkGeom chunk_geom(const void *row, int c, int V)
+{
+    constexpr int CE = kChunkBytes / E::BYTES;
+    ChunkGeom g;
+    const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row) & 15u);
+    g.h = min(mis ? static_cast<int>((16u - mis) / E::BYTES) : 0, V);
+    g.e0 = c * CE;
+    g.e1 = min(V, g.e0 + CE);
+    g.a0 = min(g.e0 + g.h, g.e1);
+    g.nb = (g.e1 - g.a0) / E::VEC;
+    g.a1 = g.a0 + g.nb * E::VEC;
+    g.n_head = g.a0 - g.e0;
+    g.n_extra = g.n_head + (g.e1 - g.a1);
+    return g;
+}
+
+// ---------------------------------------------------------- prologue -----
+// One warp per packed row: owner request (largest b with cu_rows[b] <= r),
+// position, validity and the owner's parameters.  Extra CTAs handle the
+// requests without a valid row range.
+template <typename TIn, int MODE>
+__global__ void __launch_bounds__(256) row_info_kernel(const VerifyParams p, int row_blocks)
+{
+    using E = Elt<TIn>;
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    if (static_cast<int>(blockIdx.x) >= row_blocks) {
+        const int b = (blockIdx.x - row_blocks) * 256 + threadIdx.x;
+        if (b >= p.B) return;
+        const int32_t c0 = __ldg(p.cu_rows), lo = __ldg(p.cu_rows + b), hi = __ldg(p.cu_rows + b + 1);
+        const int32_t n = hi - lo;
+        if (c0 != 0 || n < 1 || n - 1 > p.k_max || hi > p.R_cap) {
+            p.accepted_len[b] = 0;
+            p.next_token[b] = -1;
+            for (int j = 0; j <= p.k_max; ++j) p.out_tokens[static_cast<int64_t>(b) * (p.k_max + 1) + j] = -1;
+            set_status(p.status, SPEC_STATUS_BAD_ROWS);
+        }
+        return;
+    }
+    const int r = (blockIdx.x * 256 + threadIdx.x) >> 5;
+    if (r >= p.R_cap) return;
+    RowInfo inf;
+    inf.sel = 0; inf.bad = 0; inf.zd = INFINITY; inf.K = 1;
+    inf.T = 0.f; inf.top_k = 0; inf.top_p = 1.f; inf.min_p = 0.f;
+    inf.seed_lo = inf.seed_hi = inf.rid = 0;
+    int lo = 0, hi = p.B - 1;
+    while (hi > lo) {
+        const int step = (hi - lo + 31) / 32;
+        const int idx = min(lo + lane * step, hi);
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, __ldg(p.cu_rows + idx) <= r);
+        const int L = m ? 31 - __clz(m) : 0;
+        const int nlo = min(lo + L * step, hi);
+        const int nhi = (L == 31) ? hi : min(lo + (L + 1) * step - 1, hi);
+        lo = nlo;
+        hi = nhi;
+    }
+    const int b = lo;
+    const int32_t c0 = __ldg(p.cu_rows), rb = __ldg(p.cu_rows + b), re = __ldg(p.cu_rows + b + 1);
+    inf.b = b;
+    inf.pos = r - rb;
+    inf.k_b = re - rb - 1;
+    inf.valid = (c0 == 0 && rb <= r && r < re && inf.k_b >= 0 && inf.k_b <= p.k_max && re <= p.R_cap);
+    inf.draft = __ldg(p.draft_ids + r);
+    if (MODE == MODE_SAMPLE) {
+        float T = __ldg(p.temperature + b), tp = __ldg(p.top_p + b), mp = __ldg(p.min_p + b);
+        int32_t tk = __ldg(p.top_k + b);
+        if (!(T >= 0.f) || isinf(T)) { inf.bad |= SPEC_STATUS_BAD_TEMPERATURE; T = 0.f; }
+        if (tk < 0) { inf.bad |= SPEC_STATUS_BAD_TOP_K; tk = 0; }
+        if (!(tp > 0.f && tp <= 1.f)) { inf.bad |= SPEC_STATUS_BAD_TOP_P; tp = 1.f; }
+        if (!(mp >= 0.f && mp <= 1.f)) { inf.bad |= SPEC_STATUS_BAD_MIN_P; mp = 0.f; }
+        inf.T = T; inf.top_k = tk; inf.top_p = tp; inf.min_p = mp;
+        const uint64_t sd = __ldg(reinterpret_cast<const unsigned long long *>(p.seed) + b);
+        inf.seed_lo = static_cast<uint32_t>(sd);
+        inf.seed_hi = static_cast<uint32_t>(sd >> 32);
+        inf.rid = p.request_id ? __ldg(p.request_id + b) : static_cast<uint32_t>(b);
+    }
+    if (MODE == MODE_RELAXED) {
+        int32_t K = __ldg(p.relaxed_k + b);
+        if (K < 1) { inf.bad |= SPEC_STATUS_BAD_RELAXED_K; K = 1; }
+        inf.K = K;
+        const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
+        if (inf.draft >= 0 && inf.draft < p.V) inf.zd = E::load(row, inf.draft);
+    }
+    if (lane == 0) reinterpret_cast<RowInfo *>(p.ws_info)[r] = inf;
+}
+
+// ------------------------------------------------------ stream kernel ----
+// One CTA per (row, chunk); plain stores of the chunk summary only.
+template <typename TIn, int MODE>
+__global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const VerifyParams p)
+{
+    using E = Elt<TIn>;
+    constexpr int VEC = E::VEC;
+    constexpr bool HAS_INFO = (MODE != MODE_CONF);
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint4 *body = reinterpret_cast<const uint4 *>(smem);
+    Shared &sh = *reinterpret_cast<Shared *>(smem + kChunkBytes);
+    Cand *cand = reinterpret_cast<Cand *>(reinterpret_cast<uint8_t *>(&sh) + sizeof(Shared));
+    float *wbins = reinterpret_cast<float *>(cand + kCandCap);     // [kWarps][kBins] (sampler)
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nchunk = p.nchunk;
+    const int r = static_cast<int>(blockIdx.x) / nchunk;
+    const int c = static_cast<int>(blockIdx.x) - r * nchunk;
+    const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
+    const ChunkGeom g = chunk_geom<E>(row, c, p.V);
+
+    if (tid == 0) {
+        int32_t R = p.n_rows;
+        if (MODE != MODE_CONF) R = min(__ldg(p.cu_rows + p.B), p.R_cap);
+        sh.R = R;
+        sh.timeout = 0;
+        if (!HAS_INFO) {
+            RowInfo inf = {};
+            inf.b = r; inf.valid = 1;
+            sh.info = inf;
+        }
+        if (r < R) {
+            mbar_init(&sh.mbar[0], 1);
+            fence_mbar_init();
+            const uint32_t bytes = static_cast<uint32_t>(g.nb) * 16u;
+            mbar_arrive_expect_tx(&sh.mbar[0], bytes + (HAS_INFO ? 64u : 0u));
+            if (bytes) bulk_g2s(smem, row + g.a0, bytes, &sh.mbar[0]);
+            if (HAS_INFO) {
+                griddep_wait();                 // row records of the prologue
+                bulk_g2s(&sh.info, reinterpret_cast<const RowInfo *>(p.ws_info) + r, 64u, &sh.mbar[0]);
+            }
+        }
+    }
+    float xe = -INFINITY;
+    int32_t ie = INT_MAX;
+    if (tid < g.n_extra && r < p.R_cap) {
+        ie = (tid < g.n_head) ? g.e0 + tid : g.a1 + (tid - g.n_head);
+        xe = E::load(row, ie);
+        sh.extras_v[tid] = xe;
+        sh.extras_i[tid] = ie;
+    }
+    __syncthreads();
+    if (r >= sh.R) return;
+    if (tid == 0 && !mbar_wait(&sh.mbar[0], 0)) sh.timeout = 1;
+    __syncthreads();
+    const RowInfo &info = sh.info;
+    if (!info.valid) return;
+
+    // ---------------------------------------------------------- pass 1 --
+    const bool need_sum = (MODE == MODE_CONF) || (p.row_lse != nullptr);
+    const float zd = info.zd;
+    float tmax = -INFINITY, tsum = 0.f;
+    int32_t targ = INT_MAX, tcnt = 0;
+    if (need_sum) tmax = pass1_sum<E, MODE>(body, g.nb, g.a0, zd, targ, tsum, tcnt);
+    else tmax = pass1_nosum<E, MODE>(body, g.nb, g.a0, zd, targ, tsum, tcnt);
+    if (tid < g.n_extra)
+        combine(tmax, targ, tsum, tcnt, xe, ie, 1.f, (MODE == MODE_RELAXED && xe > zd) ? 1 : 0,
+                need_sum);
+    const float thread_max = tmax;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xFFFFFFFFu, tmax, o);
+        const int32_t oa = __shfl_xor_sync(0xFFFFFFFFu, targ, o);
+        const float os = __shfl_xor_sync(0xFFFFFFFFu, tsum, o);
+        const int32_t oc = __shfl_xor_sync(0xFFFFFFFFu, tcnt, o);
+        combine(tmax, targ, tsum, tcnt, om, oa, os, oc, need_sum);
+    }
+    if (lane == 0) {
+        sh.red_f[warp] = tmax; sh.red_f[kWarps + warp] = tsum;
+        sh.red_i[warp] = targ; sh.red_i[kWarps + warp] = tcnt;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float m = lane < kWarps ? sh.red_f[lane] : -INFINITY;
+        float sm_ = lane < kWarps ? sh.red_f[kWarps + lane] : 0.f;
+        int32_t a = lane < kWarps ? sh.red_i[lane] : INT_MAX;
+        int32_t cc = lane < kWarps ? sh.red_i[kWarps + lane] : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+            const int32_t oa = __shfl_xor_sync(0xFFFFFFFFu, a, o);
+            const float os = __shfl_xor_sync(0xFFFFFFFFu, sm_, o);
+            const int32_t oc = __shfl_xor_sync(0xFFFFFFFFu, cc, o);
+            combine(m, a, sm_, cc, om, oa, os, oc, need_sum);
+        }
+        if (lane == 0) {
+            sh.part.m = m; sh.part.amax = a; sh.part.s = sm_; sh.part.cnt = cc;
+            sh.part.gbest = -INFINITY; sh.part.gidx = INT_MAX; sh.part.ncand = 0;
+            sh.part.pad = 0;
+        }
+    }
+    __syncthreads();
+
+    // ------------------------------------------ sampler: chunk summary --
+    const int64_t rc = static_cast<int64_t>(r) * nchunk + c;
+    if (MODE == MODE_SAMPLE && info.T > 0.f) {
+        const float T = info.T;
+        const float invT = 1.0f / T;
+        const float sc = invT * kLog2e;
+        const bool use_k = info.top_k > 0 && info.top_k < p.V;
+        const bool use_m = info.min_p > 0.f;
+        const bool use_p = info.top_p < 1.f;
+        const bool unfiltered = !use_k && !use_m && !use_p;
+        const bool pure_p = !use_k && !use_m && use_p;
+        const float m_c = sh.part.m;
+        Cand *ws_list = reinterpret_cast<Cand *>(p.ws_cand) + rc * kCandCap;
+        float *ws_bins = p.ws_bins + rc * kBins;
+        auto visit_chunk = [&](auto &&fn, float thr) {
+            for (int i = tid; i < g.nb; i += kThreads) {
+                const uint4 v = body[i];
+                if (!(E::vmax(v) >= thr)) continue;
+                float x[VEC];
+                E::unpack(v, x);
+#pragma unroll
+                for (int q = 0; q < VEC; ++q)
+                    if (x[q] >= thr) fn(x[q], g.a0 + i * VEC + q);
+            }
+            if (tid < g.n_extra && sh.extras_v[tid] >= thr) fn(sh.extras_v[tid], sh.extras_i[tid]);
+        };
+        if (!(m_c > -INFINITY)) {
+            if (pure_p && tid < kBins) ws_bins[tid] = 0.f;
+            if (pure_p && tid == 0) sh.part.gbest = 0.f;
+        } else if (unfiltered) {
+            GumbelScorer gs{invT, static_cast<uint32_t>(info.pos), info.rid, p.step, info.seed_lo,
+                            info.seed_hi, 0xFFFFFFFFu, make_uint4(0, 0, 0, 0)};
+            float best = -INFINITY;
+            int32_t bi = INT_MAX;
+            visit_chunk([&](float v, int32_t ix) {
+                const float sv = gs(v, ix);
+                if (sv > best || (sv == best && ix < bi)) { best = sv; bi = ix; }
+            }, -INFINITY);
+            block_best(best, bi, sh);
+            if (tid == 0) { sh.part.gbest = best; sh.part.gidx = bi; }
+        } else if (pure_p) {
+            // mass exp((z - m_c)/T) per bin of T/8 below the chunk maximum;
+            // the last bin collects everything further down
+            for (int q = tid; q < kWarps * kBins; q += kThreads) wbins[q] = 0.f;
+            __syncthreads();
+            float wsum = 0.f;
+            const float bscale = kBinsPerT * invT;
+            float *mine = wbins + warp * kBins;
+            visit_chunk([&](float v, int32_t) {
+                const float d = m_c - v;
+                const float w = ex2(-d * sc);
+                wsum += w;
+                const float q = fminf(d * bscale, static_cast<float>(kBins - 1));
+                atomicAdd(mine + static_cast<int>(q), w);
+            }, -INFINITY);
+            wsum = block_sum(wsum, sh);
+            if (tid < kBins) {
+                float t = 0.f;
+                for (int w = 0; w < kWarps; ++w) t += wbins[w * kBins + tid];
+                ws_bins[tid] = t;
+            }
+            if (tid == 0) sh.part.gbest = wsum;
+        } else {
+            // lower bound of the survivor threshold within this chunk:
+            // min-p relative to the chunk maximum (<= the row maximum); for
+            // top-k a ladder level holding k thread maxima
+            float lo = use_m ? m_c + T * logf(info.min_p) : -INFINITY;
+            bool bounded = use_m;
+            if (use_k) {
+                float tlo = -INFINITY;
+                if (kth_level(thread_max, m_c, info.top_k, tlo, sh)) {
+                    lo = fmaxf(lo, tlo);
+                    bounded = true;
+                }
+            }
+            int n = INT_MAX;                     // unbounded: overflow marker
+            if (bounded) {
+                if (tid == 0) sh.cand_n = 0;
+                __syncthreads();
+                visit_chunk([&](float v, int32_t ix) {
+                    const int slot = atomicAdd(&sh.cand_n, 1);
+                    if (slot < kCandCap) { cand[slot].v = v; cand[slot].i = ix; }
+                }, lo);
+                __syncthreads();
+                n = sh.cand_n;
+                for (int i = tid; i < min(n, kCandCap); i += kThreads) ws_list[i] = cand[i];
+            }
+            if (tid == 0) sh.part.ncand = n;
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        reinterpret_cast<ChunkPart *>(p.ws_part)[rc] = sh.part;
+        if (sh.timeout) set_status(p.status, SPEC_STATUS_TIMEOUT);
+    }
+}
+
+// ------------------------------------------------------ finish kernel ----
+
+// Visit every element of a row with value >= thr as fn(value, index): the
+// aligned body streams through two shared-memory stages by TMA bulk copies
+// (phase bits in sh.ph), the unaligned head / tail use plain loads.  Called
+// by all threads of the CTA.
+template <typename E, typename F>
+__device__ void visit_row(const void *row_v, int V, int h, uint8_t *stage_mem, Shared &sh,
+                          uint32_t *ph, float thr, F &&fn)
+{
+    using T = typename std::conditional<E::BYTES == 2, uint16_t, float>::type;
+    constexpr int VEC = E::VEC;
+    constexpr int PER = kRowStage / 16;
+    const T *row = reinterpret_cast<const T *>(row_v);
+    const int tid = threadIdx.x;
+    const int nv = (V - h) / VEC;
+    const int npieces = (nv + PER - 1) / PER;
+    const uint4 *src = reinterpret_cast<const uint4 *>(row + h);
+    auto issue = [&](int q) {
+        const int s = q & 1;
+        const uint32_t bytes = static_cast<uint32_t>(min(PER, nv - q * PER)) * 16u;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&sh.mbar[s], bytes);
+        bulk_g2s(stage_mem + s * kRowStage, src + static_cast<int64_t>(q) * PER, bytes, &sh.mbar[s]);
+    };
+    if (tid == 0)
+        for (int q = 0; q < min(2, npieces); ++q) issue(q);
+    for (int q = 0; q < npieces; ++q) {
+        const int s = q & 1;
+        if (tid == 0 && !mbar_wait(&sh.mbar[s], ph[s])) sh.timeout = 1;
+        __syncthreads();
+        const uint4 *buf = reinterpret_cast<const uint4 *>(stage_mem + s * kRowStage);
+        const int n = min(PER, nv - q * PER), base = h + q * PER * VEC;
+        for (int i = tid; i < n; i += kThreads) {
+            const uint4 v = buf[i];
+            if (!(E::vmax(v) >= thr)) continue;
+            float x[VEC];
+            E::unpack(v, x);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                if (x[j] >= thr) fn(x[j], base + i * VEC + j);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            ph[s] ^= 1u;
+            if (q + 2 < npieces) issue(q + 2);
+        }
+    }
+    const int t0 = h + nv * VEC;
+    if (tid < h) { const float v = E::load(row, tid); if (v >= thr) fn(v, tid); }
+    if (tid < V - t0) { const float v = E::load(row, t0 + tid); if (v >= thr) fn(v, t0 + tid); }
+}
+
+// One CTA per packed row, after the stream kernel: combine the chunk
+// summaries, pick the row's token, write the row results, run the chain.
+template <typename TIn, int MODE>
+__global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParams p)
+{
+    using E = Elt<TIn>;
+    constexpr int VEC = E::VEC;
+    constexpr int PASSES = (sizeof(TIn) == 2) ? 2 : 4;
+    extern __shared__ __align__(128) uint8_t smem[];
+    Shared &sh = *reinterpret_cast<Shared *>(smem);
+    ChunkPart *parts = reinterpret_cast<ChunkPart *>(smem + sizeof(Shared));       // [kMaxChunks]
+    Cand *band = reinterpret_cast<Cand *>(parts + kMaxChunks);                     // [kBandCap]
+    uint8_t *stage_mem = reinterpret_cast<uint8_t *>(band + kBandCap);             // 2 x kRowStage
+    __shared__ uint32_t ph[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = blockIdx.x;
+    const int nchunk = p.nchunk;
+
+    griddep_wait();                        // the stream kernel's stores are visible
+    if (tid == 0) {
+        if (MODE != MODE_CONF) {
+            sh.info = reinterpret_cast<const RowInfo *>(p.ws_info)[r];
+            sh.info.valid = sh.info.valid && r < min(__ldg(p.cu_rows + p.B), p.R_cap);
+        } else {
+            RowInfo inf = {};
+            inf.b = r; inf.valid = 1;
+            inf.sel = p.selected ? static_cast<uint32_t>(__ldg(p.selected + r)) : 0xFFFFFFFFu;
+            sh.info = inf;
+        }
+        sh.timeout = 0;
+        mbar_init(&sh.mbar[0], 1);
+        mbar_init(&sh.mbar[1], 1);
+        fence_mbar_init();
+        ph[0] = ph[1] = 0u;
+    }
+    if (tid < nchunk) {
+        const ChunkPart *rp = reinterpret_cast<const ChunkPart *>(p.ws_part) + static_cast<int64_t>(r) * nchunk;
+        const float4 a = __ldcg(reinterpret_cast<const float4 *>(rp + tid));
+        const float4 b = __ldcg(reinterpret_cast<const float4 *>(rp + tid) + 1);
+        ChunkPart cp;
+        cp.m = a.x; cp.amax = __float_as_int(a.y); cp.s = a.z; cp.cnt = __float_as_int(a.w);
+        cp.gbest = b.x; cp.gidx = __float_as_int(b.y); cp.ncand = __float_as_int(b.z); cp.pad = 0;
+        parts[tid] = cp;
+    }
+    __syncthreads();
+    const RowInfo &info = sh.info;
+    if (!info.valid) return;
+    const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
+    const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row) & 15u);
+    const int h = min(mis ? static_cast<int>((16u - mis) / E::BYTES) : 0, p.V);
+    const bool need_sum = (MODE == MODE_CONF) || (p.row_lse != nullptr);
+
+    // combine the chunk summaries (warp 0; chunk order fixed)
+    if (warp == 0) {
+        float m = -INFINITY, s = 0.f;
+        int32_t a = INT_MAX, cc = 0;
+        for (int q = lane; q < nchunk; q += 32)
+            combine(m, a, s, cc, parts[q].m, parts[q].amax, parts[q].s, parts[q].cnt, need_sum);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+            const int32_t oa = __shfl_xor_sync(0xFFFFFFFFu, a, o);
+            const float os = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+            const int32_t oc = __shfl_xor_sync(0xFFFFFFFFu, cc, o);
+            combine(m, a, s, cc, om, oa, os, oc, need_sum);
+        }
+        if (lane == 0) {
+            sh.M = m; sh.S = s; sh.CNT = cc;
+            sh.AMAX = (m == -INFINITY) ? 0 : a;
+        }
+    }
+    __syncthreads();
+    const float M = sh.M;
+    const int32_t AMAX = sh.AMAX;
+    int32_t y = AMAX;
+    int32_t flag = 0;
+    if (MODE == MODE_RELAXED)
+        flag = (info.draft >= 0 && info.draft < p.V && sh.CNT < info.K) ? 1 : 0;
+
+    if (MODE == MODE_SAMPLE && info.T > 0.f && M > -INFINITY) {
+        const float T = info.T;
+        const float invT = 1.0f / T;
+        const float sc = invT * kLog2e;
+        const bool use_k = info.top_k > 0 && info.top_k < p.V;
+        const bool use_m = info.min_p > 0.f;
+        const bool use_p = info.top_p < 1.f;
+        const bool unfiltered = !use_k && !use_m && !use_p;
+        const bool pure_p = !use_k && !use_m && use_p;
+        GumbelScorer gs{invT, static_cast<uint32_t>(info.pos), info.rid, p.step, info.seed_lo,
+                        info.seed_hi, 0xFFFFFFFFu, make_uint4(0, 0, 0, 0)};
+        float best = -INFINITY;
+        int32_t bi = INT_MAX;
+        if (unfiltered) {
+            for (int q = tid; q < nchunk; q += kThreads) {
+                const float gb = parts[q].gbest;
+                const int32_t gi = parts[q].gidx;
+                if (gb > best || (gb == best && gi < bi)) { best = gb; bi = gi; }
+            }
+            block_best(best, bi, sh);
+        } else if (pure_p) {
+            // W from the chunk sums; bracket the nucleus boundary with the
+            // chunk bins: with levels L_k = k/8 (units of T below M),
+            //   LB(L) = mass of bins lying wholly within distance < L,
+            //   UB(L) = mass of bins starting at a distance < L;
+            // values at distance <= L_in (UB(L_in) < top_p W) are in the
+            // nucleus, values at distance >= L_out (LB(L_out) >= top_p W) are
+            // out; the band between is settled exactly.
+            float *cum = reinterpret_cast<float *>(band);           // [nchunk][kBins] prefix sums
+            const float *rb = p.ws_bins + static_cast<int64_t>(r) * nchunk * kBins;
+            for (int q = tid; q < nchunk * kBins; q += kThreads) cum[q] = __ldcg(rb + q);
+            __syncthreads();
+            for (int q = tid; q < nchunk; q += kThreads) {
+                float run = 0.f;
+                for (int j = 0; j < kBins; ++j) { run += cum[q * kBins + j]; cum[q * kBins + j] = run; }
+            }
+            if (tid == 0) {
+                float w = 0.f;
+                for (int q = 0; q < nchunk; ++q)
+                    if (parts[q].m > -INFINITY) w += parts[q].gbest * ex2((parts[q].m - M) * sc);
+                sh.W = w;
+            }
+            __syncthreads();
+            const float W = sh.W, target = info.top_p * W;
+            // thread t evaluates level L = t / kBinsPerT (t = 0..255)
+            const float L = static_cast<float>(tid) / kBinsPerT;
+            float lb = 0.f, ub = 0.f;
+            for (int q = 0; q < nchunk; ++q) {
+                const float mq = parts[q].m;
+                if (!(mq > -INFINITY)) continue;
+                const float delta = (M - mq) * invT;
+                const float fac = ex2((mq - M) * sc);
+                // bins j < kBins-1 cover [delta + j/8, delta + (j+1)/8); the last
+                // bin covers [delta + (kBins-1)/8, inf)
+                const float u = (L - delta) * kBinsPerT;
+                const int j_lb = static_cast<int>(fminf(floorf(u), static_cast<float>(kBins - 1))) - 1;
+                const int j_ub = static_cast<int>(fminf(ceilf(u), static_cast<float>(kBins))) - 1;
+                if (j_lb >= 0) lb += cum[q * kBins + j_lb] * fac;
+                if (j_ub >= 0) ub += cum[q * kBins + min(j_ub, kBins - 1)] * fac;
+            }
+            int *flags = reinterpret_cast<int *>(sh.hist);
+            flags[tid] = (ub < target ? 1 : 0) | (lb >= target ? 2 : 0);
+            __syncthreads();
+            if (tid == 0) {
+                int kin = -1, kout = -1;
+                for (int t = 0; t < kThreads; ++t) {
+                    if (flags[t] & 1) kin = t;
+                    if ((flags[t] & 2) && kout < 0) kout = t;
+                }
+                sh.band_lo = kin;
+                sh.band_hi = kout;
+            }
+            __syncthreads();
+            const float eps = 1e-3f;
+            const float din = (sh.band_lo < 0) ? -1.f : static_cast<float>(sh.band_lo) / kBinsPerT - eps;
+            const float dout = (sh.band_hi < 0) ? INFINITY : static_cast<float>(sh.band_hi) / kBinsPerT + eps;
+            // one pass over the row: Gumbel-max over the sure part, exact mass
+            // of the sure part, the band collected on chip
+            if (tid == 0) sh.cand_n = 0;
+            __syncthreads();
+            float mass_in = 0.f;
+            const float thr = (dout == INFINITY) ? -INFINITY : M - dout * T;
+            visit_row<E>(row, p.V, h, stage_mem, sh, ph, thr, [&](float v, int32_t ix) {
+                const float d = (M - v) * invT;
+                if (d <= din) {
+                    mass_in += ex2((v - M) * sc);
+                    const float sv = gs(v, ix);
+                    if (sv > best || (sv == best && ix < bi)) { best = sv; bi = ix; }
+                } else if (d < dout) {
+                    const int slot = atomicAdd(&sh.cand_n, 1);
+                    if (slot < kBandCap) { band[slot].v = v; band[slot].i = ix; }
+                }
+            });
+            mass_in = block_sum(mass_in, sh);
+            const int nband = sh.cand_n;
+            if (nband <= kBandCap) {
+                if (nband > 0) {
+                    auto visit_band = [&](auto &&fn, float t2) {
+                        for (int i = tid; i < nband; i += kThreads)
+                            if (band[i].v >= t2) fn(band[i].v, band[i].i);
+                    };
+                    const float tgt = target - mass_in;
+                    uint32_t kF = 0u;
+                    if (tgt > 0.f) kF = radix_select<true>(visit_band, 0u, tgt, 0u, M, sc, PASSES, sh);
+                    else kF = 0xFFFFFFFFu;           // the sure part already holds the mass
+                    visit_band([&](float v, int32_t ix) {
+                        if (fkey(v) < kF) return;
+                        const float sv = gs(v, ix);
+                        if (sv > best || (sv == best && ix < bi)) { best = sv; bi = ix; }
+                    }, -INFINITY);
+                }
+            } else {
+                // band too large: exact mass select over the whole row
+                best = -INFINITY;
+                bi = INT_MAX;
+                auto visit_all = [&](auto &&fn, float t2) {
+                    visit_row<E>(row, p.V, h, stage_mem, sh, ph, t2, fn);
+                };
+                const uint32_t kF = radix_select<true>(visit_all, 0u, target, 0u, M, sc, PASSES, sh);
+                visit_all([&](float v, int32_t ix) {
+                    if (fkey(v) < kF) return;
+                    const float sv = gs(v, ix);
+                    if (sv > best || (sv == best && ix < bi)) { best = sv; bi = ix; }
+                }, key_floor(kF));
+            }
+            block_best(best, bi, sh);
+        } else {
+            // top-k and / or min-p: candidates from the chunk lists, or from
+            // the row itself when a list overflowed
+            const float th_m = use_m ? M + T * logf(info.min_p) : -INFINITY;
+            if (tid == 0) {
+                int tot = 0, ovf = 0;
+                for (int q = 0; q < nchunk; ++q) {
+                    const int nq = parts[q].ncand;
+                    ovf |= (nq > kCandCap);
+                    tot += min(nq, kCandCap);
+                }
+                sh.total = tot;
+                sh.overflow = ovf;
+            }
+            __syncthreads();
+            const bool whole = sh.overflow != 0;
+            const int n_list = sh.total;
+            auto visit = [&](auto &&fn, float thr) {
+                if (whole) {
+                    visit_row<E>(row, p.V, h, stage_mem, sh, ph, thr, fn);
+                } else {
+                    int base = 0;
+                    for (int q = 0; q < nchunk; ++q) {
+                        const int nq = min(parts[q].ncand, kCandCap);
+                        const float2 *lq = reinterpret_cast<const float2 *>(p.ws_cand) +
+                                           (static_cast<int64_t>(r) * nchunk + q) * kCandCap;
+                        for (int i = ((tid - base) % kThreads + kThreads) % kThreads; i < nq; i += kThreads) {
+                            const float2 e = __ldcg(lq + i);
+                            if (e.x >= thr) fn(e.x, __float_as_int(e.y));
+                        }
+                        base += nq;
+                    }
+                }
+            };
+            uint32_t key_S = use_m ? fkey(th_m) : 0u;
+            if (use_k && (whole || n_list >= info.top_k))
+                key_S = max(key_S, radix_select<false>(visit, key_S, 0.f,
+                                                       static_cast<uint32_t>(info.top_k), M, sc,
+                                                       PASSES, sh));
+            uint32_t key_F = key_S;
+            if (use_p) {
+                float w = 0.f;
+                const uint32_t kS = key_S;
+                visit([&](float v, int32_t) {
+                    if (fkey(v) >= kS) w += ex2((v - M) * sc);
+                }, key_floor(key_S));
+                const float W = block_sum(w, sh);
+                key_F = max(key_S, radix_select<true>(visit, key_S, info.top_p * W, 0u, M, sc,
+                                                      PASSES, sh));
+            }
+            const uint32_t kF = key_F;
+            visit([&](float v, int32_t ix) {
+                if (fkey(v) < kF) return;
+                const float sv = gs(v, ix);
+                if (sv > best || (sv == best && ix < bi)) { best = sv; bi = ix; }
+            }, key_floor(key_F));
+            block_best(best, bi, sh);
+        }
+        y = (bi == INT_MAX) ? AMAX : bi;
+    }
+
+    // ---------------------------------------------------- row results ---
+    if (tid == 0) {
+        const float S = sh.S;
+        if (p.row_max) p.row_max[r] = M;
+        if (p.row_lse) p.row_lse[r] = (S > 0.f) ? M + logf(S) : -INFINITY;
+        if (p.row_argmax) p.row_argmax[r] = AMAX;
+        if (MODE == MODE_CONF) {
+            const int32_t s = p.selected ? static_cast<int32_t>(info.sel) : AMAX;
+            float cf = 0.f;
+            if (s >= 0 && s < p.V) {
+                const float zs = E::load(row, s);
+                cf = (S > 0.f) ? ex2((zs - M) * kLog2e) / S : 0.f;
+            } else {
+                set_status(p.status, SPEC_STATUS_BAD_SELECTED);
+            }
+            p.conf[r] = cf;
+            p.draft_token[r] = s;
+        } else {
+            if (p.row_token) p.row_token[r] = y;
+            p.ws_tok[r] = y;
+            if (MODE == MODE_RELAXED) p.ws_flag[r] = flag;
+        }
+        if (sh.timeout) set_status(p.status, SPEC_STATUS_TIMEOUT);
+    }
+
+    // ------------------------------- request chain (last row of request) --
+    if (MODE != MODE_CONF && warp == 0) {
+        uint32_t t = 0;
+        if (lane == 0) {
+            fence_acq_rel_gpu();
+            t = atomicAdd(p.ws_ticket + info.b, 1u);
+            if (t == static_cast<uint32_t>(info.k_b)) fence_acq_rel_gpu();
+        }
+        t = __shfl_sync(0xFFFFFFFFu, t, 0);
+        if (t == static_cast<uint32_t>(info.k_b)) {
+            const int b = info.b, k = info.k_b, r0 = r - info.pos;
+            const int j = lane;
+            const int32_t yj = (j <= k) ? __ldcg(p.ws_tok + r0 + j) : -1;
+            const int32_t dj = (j < k) ? __ldg(p.draft_ids + r0 + j) : -1;
+            bool ok;
+            if (MODE == MODE_RELAXED) ok = (j < k) && __ldcg(p.ws_flag + r0 + j) != 0;
+            else ok = (j < k) && (yj == dj);
+            const unsigned mism = __ballot_sync(0xFFFFFFFFu, (j < k) && !ok);
+            const int a = mism ? (__ffs(mism) - 1) : k;
+            const int32_t tok = __shfl_sync(0xFFFFFFFFu, yj, a);
+            if (j <= p.k_max)
+                p.out_tokens[static_cast<int64_t>(b) * (p.k_max + 1) + j] = (j < a) ? dj : (j == a ? tok : -1);
+            if (j == 0) {
+                p.accepted_len[b] = a;
+                p.next_token[b] = tok;
+                p.ws_ticket[b] = 0u;
+                set_status(p.status, static_cast<uint32_t>(info.bad));
+                if (p.hist) atomicAdd(reinterpret_cast<unsigned long long *>(p.hist + a), 1ull);
+            }
+            if (j < p.k_max) {
+                if (p.acc && a > j) atomicAdd(reinterpret_cast<unsigned long long *>(p.acc + j), 1ull);
+                if (p.ver && k > j) atomicAdd(reinterpret_cast<unsigned long long *>(p.ver + j), 1ull);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------- host -----
+
+int chunks_per_row(int32_t V, int elt)
+{
+    const int64_t ce = kChunkBytes / elt;
+    return static_cast<int>((static_cast<int64_t>(V) + ce - 1) / ce);
+}
+
+size_t max_row_bytes() { return static_cast<size_t>(kMaxChunks) * kChunkBytes; }
+
+template <typename TIn, int MODE>
+static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
+{
+    size_t smem = kChunkBytes + sizeof(Shared);
+    if (MODE == MODE_SAMPLE)
+        smem += static_cast<size_t>(kCandCap) * sizeof(Cand) + static_cast<size_t>(kWarps) * kBins * 4;
+    const size_t smem_fin = sizeof(Shared) + kMaxChunks * sizeof(ChunkPart) +
+                            static_cast<size_t>(kBandCap) * sizeof(Cand) + 2 * kRowStage;
+    auto kstream = stream_chunks_kernel<TIn, MODE>;
+    auto kfin = finish_rows_kernel<TIn, MODE>;
+    // raise the dynamic shared-memory limits once per device
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !done[dev]) {
+        e = cudaFuncSetAttribute(kstream, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kfin, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem_fin));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) done[dev] = true;
+    }
+    const int rows = (MODE == MODE_CONF) ? p.n_rows : p.R_cap;
+    if (MODE != MODE_CONF) {
+        const int row_blocks = static_cast<int>((static_cast<int64_t>(p.R_cap) * 32 + 255) / 256);
+        const int req_blocks = (p.B + 255) / 256;
+        row_info_kernel<TIn, MODE><<<row_blocks + req_blocks, 256, 0, stream>>>(p, row_blocks);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(rows) * static_cast<unsigned>(p.nchunk), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = (MODE != MODE_CONF) ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kstream, p);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cf = {};
+    cf.gridDim = dim3(static_cast<unsigned>(rows), 1, 1);
+    cf.blockDim = dim3(kThreads, 1, 1);
+    cf.dynamicSmemBytes = smem_fin;
+    cf.stream = stream;
+    cf.attrs = attr;
+    cf.numAttrs = 1;
+    return cudaLaunchKernelEx(&cf, kfin, p);
+}
+
+cudaError_t launch_verify(int mode, int dtype, const VerifyParams &p, cudaStream_t stream)
+{
+    if (dtype == SPEC_BF16) {
+        switch (mode) {
+        case MODE_GREEDY: return launch_t<uint16_t, MODE_GREEDY>(p, stream);
+        case MODE_RELAXED: return launch_t<uint16_t, MODE_RELAXED>(p, stream);
+        case MODE_SAMPLE: return launch_t<uint16_t, MODE_SAMPLE>(p, stream);
+        case MODE_CONF: return launch_t<uint16_t, MODE_CONF>(p, stream);
+        }
+    } else {
+        switch (mode) {
+        case MODE_GREEDY: return launch_t<float, MODE_GREEDY>(p, stream);
+        case MODE_RELAXED: return launch_t<float, MODE_RELAXED>(p, stream);
+        case MODE_SAMPLE: return launch_t<float, MODE_SAMPLE>(p, stream);
+        case MODE_CONF: return launch_t<float, MODE_CONF>(p, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace specv
