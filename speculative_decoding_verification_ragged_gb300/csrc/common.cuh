@@ -236,12 +236,10 @@ __device__ __forceinline__ float gumbel_of(uint32_t x)
 {
     const float u = __uint_as_float((x >> 9) | 0x3F800000u) - __uint_as_float(0x3F7FFFFFu);
     const float d = __uint_as_float(((~x) >> 9) | 0x3F800000u) - __uint_as_float(0x3F7FFFFFu);
-    float e;
-    if (d < 0.03125f) {
-        e = d * fmaf(d, fmaf(d, fmaf(d, fmaf(d, 0.2f, 0.25f), 1.0f / 3.0f), 0.5f), 1.0f);
-    } else {
-        e = -kLn2 * lg2(u);
-    }
+    // both forms evaluated and selected: no divergent branch in a warp
+    const float e_series = d * fmaf(d, fmaf(d, fmaf(d, fmaf(d, 0.2f, 0.25f), 1.0f / 3.0f), 0.5f), 1.0f);
+    const float e_log = -kLn2 * lg2(u);
+    const float e = (d < 0.03125f) ? e_series : e_log;
     return -kLn2 * lg2(e);
 }
 

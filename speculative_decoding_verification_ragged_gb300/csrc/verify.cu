@@ -8,32 +8,39 @@
 //     cu_rows), the row's position and validity and the owner's parameters,
 //     as a 64-byte row record; requests without a valid row range get their
 //     outputs here.
-//   stream, one CTA per (row, chunk of kChunkBytes): thread 0 stages the
-//     chunk's 16-byte-aligned body in shared memory with one 1-D TMA bulk
-//     copy and the row record with a second, on one mbarrier (the row is read
-//     from HBM exactly once; unaligned head/tail elements use plain loads).
-//     Pass 1 runs a per-thread online max / first argmax / sum exp(z - max)
-//     over 16-byte vectors (packed bf16x2 max per vector; two independent
-//     accumulators), plus the count of logits above the draft's logit for
-//     relaxed top-K; warp shuffles and a CTA reduction give the chunk
-//     summary.  For the sampler (T > 0) the survivors form an upper set
-//     {z >= th}: with top-k or min-p the chunk bounds th from below (chunk max
-//     + T ln min_p; a ladder level below the chunk max holding k thread
-//     maxima) and stores the elements above the bound as candidates; with no
-//     filter it stores its own Gumbel-max winner; with pure top-p it stores
-//     its mass exp((z - m_c)/T) in bins of T/8 below its maximum.  Only plain
-//     stores: nothing in this kernel waits for, or fences against, another
-//     CTA.
-//   finish, one CTA per row: combine the chunk summaries in parallel, then
-//     for the sampler run 8-bit radix selects (exact k-th largest value,
-//     exact top-p mass crossing) over the candidates and Gumbel-max over the
-//     survivors with Philox4x32-10 uniforms.  Pure top-p brackets the nucleus
-//     boundary with the chunk bins and settles it exactly on the one band of
-//     values the bins cannot decide, from a single pass over the row (L2)
-//     streamed through shared memory by TMA.  The CTA finishing the last row
-//     of a request (atomic ticket) runs the accept-while-equal prefix scan
-//     with one warp ballot and writes the request's tokens and the optional
-//     prefix-acceptance counters.
+//   stream, one CTA per (row, chunk of kChunkBytes): thread 0 first issues
+//     one 1-D TMA bulk copy of the chunk's 16-byte-aligned body into shared
+//     memory, then a second one of the row record on the same mbarrier (the
+//     row is read from HBM exactly once; unaligned head/tail elements use
+//     plain loads).  Pass 1 runs a per-thread online max / first argmax /
+//     sum exp(z - max) over 16-byte vectors, plus the count of logits above
+//     the draft's logit for relaxed top-K; warp shuffles and a CTA reduction
+//     give the chunk summary.  For the sampler (T > 0):
+//       no filter   - the chunk's own Gumbel-max winner (vectors that cannot
+//                     beat a lower bound taken from the thread maxima are
+//                     skipped);
+//       top-k/min-p - the survivors form an upper set {z >= th}; the chunk
+//                     bounds th from below (exact k-th largest of the thread
+//                     maxima; chunk max + T ln min_p) and stores the elements
+//                     above the bound as candidates;
+//       top-p only  - the mass exp((z - m_c)/T) in bins of an absolute grid
+//                     floor(z * 8/T) (per-warp fixed-point integer sums, each
+//                     bin scaled by its own distance so the precision is
+//                     relative), the total mass, and a candidate list above
+//                     the 64-th largest thread maximum.
+//     Only plain stores: nothing in this kernel waits for, or fences
+//     against, another CTA.
+//   finish, one CTA per row: combine the chunk summaries, then for the
+//     sampler run radix selects (exact k-th largest value, exact top-p mass
+//     crossing) over the candidate lists staged in shared memory and
+//     Gumbel-max over the survivors with Philox4x32-10 uniforms.  Pure top-p
+//     brackets the nucleus boundary with the combined bins and settles it
+//     exactly on the one band of bins the bracket cannot decide, from the
+//     candidate lists when they cover the band, else from one pass over the
+//     row streamed through shared memory by TMA.  The CTA finishing the last
+//     row of a request (atomic ticket) runs the accept-while-equal prefix
+//     scan with one warp ballot and writes the request's tokens and the
+//     optional prefix-acceptance counters.
 //
 // Definitions: xLLM docs "自适应投机推理" §"启动示例" (ragged rejection
 // sampler with packed-row owners, point-mass draft, replacement / bonus,
@@ -54,8 +61,16 @@ namespace specv {
 constexpr int kCandCap = kWsCandCap;    // candidates one chunk may store
 constexpr int kBins = kWsBins;          // pure top-p mass bins per chunk
 constexpr float kBinsPerT = 8.0f;       // bin width T/8
-constexpr int kBandCap = 4096;          // undecided values the finish kernel keeps on chip
+constexpr float kFix = 1048576.0f;      // fixed-point scale of one bin weight (2^20)
+constexpr int32_t kNoBins = INT_MIN;    // chunk grid origin too large for exact bins
+constexpr int kBandCap = 2048;          // undecided values the finish kernel keeps on chip
+constexpr int kListCap = 2048;          // candidates the finish kernel stages on chip
 constexpr int kRowStage = 16 * 1024;    // finish kernel: bytes per row-streaming stage
+constexpr int kPureListK = 64;          // pure top-p: list above the 64-th thread maximum
+constexpr float kMassTol = 1e-5f;       // relative slack of the bin bracket
+// Largest Gumbel noise of the uniform lattice: u <= 1 - 2^-24 gives
+// -log(-log u) <= 24 ln 2 = 16.636; the bound used leaves a margin.
+constexpr float kGumbelMax = 16.75f;
 
 // row record written by the prologue (64 bytes)
 struct __align__(16) RowInfo {
@@ -72,11 +87,13 @@ struct __align__(16) ChunkPart {
     int32_t amax;   // first argmax in the chunk
     float s;        // sum exp(z - m)
     int32_t cnt;    // relaxed: logits above the draft's
-    float gbest;    // sampler, no filter: best Gumbel score; pure top-p: mass sum
-    int32_t gidx;   //   and its index
+    float gbest;    // sampler, no filter: best Gumbel score; top-p only: chunk mass
+    int32_t gidx;   //   and its index; top-p only: bin-grid origin floor(m * 8/T)
     int32_t ncand;  // sampler with a bound: candidates (> kCandCap: overflow)
-    int32_t pad;
+    float lev;      // sampler with a bound: the level the candidates lie above
 };
+static_assert(sizeof(ChunkPart) == 32, "chunk summary is 32 bytes");
+static_assert(kListCap * 8 <= 2 * kRowStage, "lists fit in the row stages");
 
 // shared scratch common to both row kernels
 struct __align__(16) Shared {
@@ -86,9 +103,10 @@ struct __align__(16) Shared {
     uint32_t scan[kWarps];
     float red_f[kWarps * 2];
     int32_t red_i[kWarps * 2];
-    float M, S, W, sel_t, sel_excl_f, excl_band;
-    int32_t AMAX, CNT, sel_bin, sel_found, total, overflow, cand_n, R, band_lo, band_hi;
-    uint32_t sel_excl_u;
+    int32_t offs[kMaxChunks + 1];
+    float M, S, W, sel_excl_f, theta;
+    int32_t AMAX, CNT, sel_bin, sel_found, total, overflow, cand_n, R, J, nobins;
+    uint32_t sel_excl_u, lkey;
     float extras_v[16];
     int32_t extras_i[16];
     int32_t timeout;
@@ -162,42 +180,61 @@ __device__ void find_crossing(const V *hist, V target, Shared &sh)
     }
 }
 
-// final 32-bit key from the 8-bit digits chosen (bf16 keys use bits 31..16)
-__device__ __forceinline__ uint32_t finish_key(uint32_t prefix, int passes)
-{
-    if (passes == 2) return (prefix << 16) | ((prefix & 0x8000u) ? 0u : 0xFFFFu);
-    return prefix;
-}
-
 // Float threshold equivalent to "key >= k": -inf for the keys below -inf's.
 __device__ __forceinline__ float key_floor(uint32_t k)
 {
     return (k <= 0x007FFFFFu) ? -INFINITY : key_value(k);
 }
 
-// CTA-local radix select over the values produced by `visit(fn, thr)` (fn(v,
-// i) for every element >= thr): the key of the k-th largest value, or of the
-// value group where the cumulative weight exp((z - M) * sc) counted from the
-// top first reaches `target`.  Only values with key >= key_min take part.
-template <bool MASS, typename Visit>
-__device__ uint32_t radix_select(Visit &&visit, uint32_t key_min, float target, uint32_t k,
-                                 float M, float sc, int passes, Shared &sh)
+// Radix select over the keys of the values produced by `visit(fn, thr)`
+// (fn(v, i) for every element >= thr).  Values are compared through their
+// order-preserving keys; bf16 values have 16 significant key bits, fp32 32.
+// Only keys in [lo, hi] take part (hi must bound every such key from above).
+// Digits of 8 bits start at the highest bit where lo and hi differ.
+//   COUNT (MASS = false): the key of the k-th largest value.
+//   MASS: the key of the value group where the cumulative weight
+//     exp((z - M) * sc), counted from the top, first reaches `target`.
+// On the last digit every bin holds one value, so the weights there come
+// from integer counts (no float atomics).
+template <typename E, bool MASS, typename Visit>
+__device__ uint32_t select_key(Visit &&visit, uint32_t lo, uint32_t hi, float target, uint32_t k,
+                               float M, float sc, Shared &sh)
 {
-    uint32_t prefix = 0;
-    const float thr = key_floor(key_min);
-    for (int pass = 0; pass < passes; ++pass) {
-        const int shift = 24 - 8 * pass;
-        sh.hist[threadIdx.x] = 0u;
+    constexpr int VS = (E::BYTES == 2) ? 16 : 0;
+    const uint32_t vlo = lo >> VS, vhi = hi >> VS;
+    const uint32_t x = vlo ^ vhi;
+    int shift = x ? ((31 - __clz(x)) / 8) * 8 : 0;
+    uint32_t prefix = (shift + 8 >= 32) ? 0u : (vhi >> (shift + 8));
+    const float thr = key_floor(lo);
+    const int t = threadIdx.x;
+    for (;;) {
+        sh.hist[t] = 0u;
         __syncthreads();
+        const int sh8 = shift + 8;
+        const bool wide = MASS && shift > 0;
         visit([&](float v, int32_t) {
-            const uint32_t key = fkey(v);
-            if (key < key_min) return;
-            if (pass > 0 && (key >> (shift + 8)) != prefix) return;
-            const uint32_t bin = (key >> shift) & 255u;
-            if (MASS) atomicAdd(reinterpret_cast<float *>(&sh.hist[bin]), ex2((v - M) * sc));
+            const uint32_t fk = fkey(v);
+            if (fk < lo) return;
+            const uint32_t vk = fk >> VS;
+            if (sh8 < 32 && (vk >> sh8) != prefix) return;
+            const uint32_t bin = (vk >> shift) & 255u;
+            if (wide) atomicAdd(reinterpret_cast<float *>(&sh.hist[bin]), ex2((v - M) * sc));
             else atomicAdd(&sh.hist[bin], 1u);
         }, thr);
         __syncthreads();
+        if (MASS && shift == 0) {
+            // one value per bin: weight = count * exp((value - M) * sc)
+            const uint32_t c = sh.hist[t];
+            float w = 0.f;
+            if (c) {
+                const uint32_t vk = (prefix << 8) | static_cast<uint32_t>(t);
+                const uint32_t fk = VS ? ((vk << 16) | ((vk & 0x8000u) ? 0u : 0xFFFFu)) : vk;
+                w = static_cast<float>(c) * ex2((key_value(fk) - M) * sc);
+            }
+            __syncthreads();
+            reinterpret_cast<float *>(sh.hist)[t] = w;
+            __syncthreads();
+        }
         if (MASS) find_crossing<float>(reinterpret_cast<const float *>(sh.hist), target, sh);
         else find_crossing<uint32_t>(sh.hist, k, sh);
         const int bin = sh.sel_bin;
@@ -205,8 +242,11 @@ __device__ uint32_t radix_select(Visit &&visit, uint32_t key_min, float target, 
         else k -= sh.sel_excl_u;
         prefix = (prefix << 8) | static_cast<uint32_t>(bin < 0 ? 0 : bin);
         __syncthreads();
+        if (shift == 0) break;
+        shift -= 8;
     }
-    return finish_key(prefix, passes);
+    if (VS) return (prefix << 16) | ((prefix & 0x8000u) ? 0u : 0xFFFFu);
+    return prefix;
 }
 
 // block reduction of a float sum (result in every thread)
@@ -240,10 +280,33 @@ __device__ __forceinline__ void block_best(float &best, int32_t &bi, Shared &sh)
     __syncthreads();
 }
 
-// Top-k bound inside a chunk: the highest level L = m_c - D (D from a fixed
-// ladder) with at least k thread maxima >= L.  Thread maxima are distinct
-// elements, so at least k elements of the chunk are >= L and the chunk's
-// share of the row's top k lies above it.  False if no level qualifies.
+// block minimum and maximum of a key (result in every thread)
+__device__ __forceinline__ void block_minmax(uint32_t &mn, uint32_t &mx, Shared &sh)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        sh.red_i[threadIdx.x >> 5] = static_cast<int32_t>(mn);
+        sh.red_i[kWarps + (threadIdx.x >> 5)] = static_cast<int32_t>(mx);
+    }
+    __syncthreads();
+    mn = 0xFFFFFFFFu;
+    mx = 0u;
+    for (int q = 0; q < kWarps; ++q) {
+        mn = min(mn, static_cast<uint32_t>(sh.red_i[q]));
+        mx = max(mx, static_cast<uint32_t>(sh.red_i[kWarps + q]));
+    }
+    __syncthreads();
+}
+
+// Top-k bound inside a chunk for k above the thread count: the highest level
+// L = m_c - D (D from a fixed ladder) with at least k thread maxima >= L.
+// Thread maxima are distinct elements, so at least k elements of the chunk
+// are >= L and the chunk's share of the row's top k lies above it.  False
+// if no level qualifies.
 __device__ __forceinline__ bool kth_level(float thread_max, float m_c, int k, float &level,
                                           Shared &sh)
 {
@@ -275,23 +338,71 @@ __device__ __forceinline__ bool kth_level(float thread_max, float m_c, int k, fl
     return true;
 }
 
-// Gumbel-perturbed score z/T - log(-log u_i), u_i from Philox4x32-10 with
-// counter (i >> 2, position, request id, step) and key (seed lo, seed hi).
+// Philox4x32-10 stream of one row: counter (i >> 2, position, request id,
+// step), key (seed lo, seed hi); element i takes word i & 3.
+struct Noise {
+    uint32_t pos, rid, step, k0, k1;
+    __device__ __forceinline__ uint4 block(uint32_t ctr) const
+    {
+        return philox4x32_10(make_uint4(ctr, pos, rid, step), k0, k1);
+    }
+    // Gumbel-perturbed score z/T - log(-log u_i) of element i
+    __device__ __forceinline__ float score(float v, int32_t ix, float invT) const
+    {
+        const uint4 w = block(static_cast<uint32_t>(ix) >> 2);
+        return fmaf(v, invT, gumbel_of(word_of(w, static_cast<uint32_t>(ix) & 3u)));
+    }
+};
+
+// keep the better of (s, ix) and (best, bi): higher score, lower index on ties
+__device__ __forceinline__ void keep_best(float s, int32_t ix, float &best, int32_t &bi)
+{
+    if (s > best || (s == best && ix < bi)) { best = s; bi = ix; }
+}
+
+// scores of the VEC elements of one vector starting at element `base`, a
+// multiple of 4 (the vector covers whole Philox blocks)
+template <int VEC>
+__device__ __forceinline__ void score_vec(const float (&x)[VEC], int32_t base, float invT,
+                                          const Noise &nz, float &best, int32_t &bi)
+{
+#pragma unroll
+    for (int h = 0; h < VEC / 4; ++h) {
+        const uint4 w = nz.block((static_cast<uint32_t>(base) >> 2) + h);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            keep_best(fmaf(x[4 * h + j], invT, gumbel_of(ws[j])), base + 4 * h + j, best, bi);
+    }
+}
+
+// Gumbel scorer for elements visited one at a time; caches the last block.
 struct GumbelScorer {
     float invT;
-    uint32_t pos, rid, step, k0, k1;
+    Noise nz;
     uint32_t cached;
     uint4 words;
     __device__ __forceinline__ float operator()(float v, int32_t ix)
     {
         const uint32_t ctr = static_cast<uint32_t>(ix) >> 2;
         if (ctr != cached) {
-            words = philox4x32_10(make_uint4(ctr, pos, rid, step), k0, k1);
+            words = nz.block(ctr);
             cached = ctr;
         }
         return fmaf(v, invT, gumbel_of(word_of(words, static_cast<uint32_t>(ix) & 3u)));
     }
 };
+
+// Absolute bin of a value on the grid of width T/8: floor(z * s8), s8 = 8/T,
+// clamped.  Monotone non-decreasing in z, and computed the same way by the
+// stream and finish kernels, so both classify every value identically.
+__device__ __forceinline__ float bin_scale(float T) { return kBinsPerT / T; }
+
+__device__ __forceinline__ int32_t abs_bin(float z, float s8)
+{
+    const float f = fminf(fmaxf(floorf(z * s8), -536870912.f), 536870912.f);
+    return static_cast<int32_t>(f);
+}
 
 // Pass 1 over this thread's 16-byte vectors of the staged chunk: running max
 // with the first index attaining it, and (SUM) sum exp(z - running max)
@@ -341,20 +452,6 @@ __device__ __forceinline__ float pass1(const uint4 *body, int nb, int a0, float 
     tsum = s0 + s1;
     if (tmax == kSentinel) { tmax = -INFINITY; tsum = 0.f; }
     return tmax;
-}
-
-template <typename E, int MODE>
-__device__ __forceinline__ float pass1_sum(const uint4 *body, int nb, int a0, float zd,
-                                           int32_t &targ, float &tsum, int32_t &tcnt)
-{
-    return pass1<E, MODE, true>(body, nb, a0, zd, targ, tsum, tcnt);
-}
-
-template <typename E, int MODE>
-__device__ __forceinline__ float pass1_nosum(const uint4 *body, int nb, int a0, float zd,
-                                             int32_t &targ, float &tsum, int32_t &tcnt)
-{
-    return pass1<E, MODE, false>(body, nb, a0, zd, targ, tsum, tcnt);
 }
 
 // chunk c of a row: elements [e0, e1); 16-byte-aligned body of nb vectors
@@ -451,6 +548,20 @@ __global__ void __launch_bounds__(256) row_info_kernel(const VerifyParams p, int
 }
 
 // ------------------------------------------------------ stream kernel ----
+
+// exact k-th largest of the CTA's thread maxima (k <= kThreads): at least k
+// distinct elements of the chunk are >= it
+template <typename E>
+__device__ __forceinline__ float kth_thread_max(float thread_max, int k, float m_c, Shared &sh)
+{
+    auto visit = [&](auto &&fn, float thr) {
+        if (thread_max >= thr) fn(thread_max, 0);
+    };
+    const uint32_t key = select_key<E, false>(visit, 0u, fkey(m_c), 0.f,
+                                              static_cast<uint32_t>(k), 0.f, 0.f, sh);
+    return key_floor(key);
+}
+
 // One CTA per (row, chunk); plain stores of the chunk summary only.
 template <typename TIn, int MODE>
 __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const VerifyParams p)
@@ -462,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const Verify
     const uint4 *body = reinterpret_cast<const uint4 *>(smem);
     Shared &sh = *reinterpret_cast<Shared *>(smem + kChunkBytes);
     Cand *cand = reinterpret_cast<Cand *>(reinterpret_cast<uint8_t *>(&sh) + sizeof(Shared));
-    float *wbins = reinterpret_cast<float *>(cand + kCandCap);     // [kWarps][kBins] (sampler)
+    uint32_t *wbins = reinterpret_cast<uint32_t *>(cand + kCandCap);   // [kWarps][kBins] (sampler)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nchunk = p.nchunk;
@@ -472,39 +583,44 @@ __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const Verify
     const ChunkGeom g = chunk_geom<E>(row, c, p.V);
 
     if (tid == 0) {
-        int32_t R = p.n_rows;
-        if (MODE != MODE_CONF) R = min(__ldg(p.cu_rows + p.B), p.R_cap);
-        sh.R = R;
+        // The logits buffer holds R_cap rows, so the chunk copy is issued
+        // before anything else (in bounds even for rows past cu_rows[B]).
         sh.timeout = 0;
-        if (!HAS_INFO) {
+        mbar_init(&sh.mbar[0], 1);
+        fence_mbar_init();
+        const uint32_t bytes = static_cast<uint32_t>(g.nb) * 16u;
+        mbar_arrive_expect_tx(&sh.mbar[0], bytes + (HAS_INFO ? 64u : 0u));
+        if (bytes) bulk_g2s(smem, row + g.a0, bytes, &sh.mbar[0]);
+        int32_t R = p.n_rows;
+        if (MODE != MODE_CONF) R = __ldg(p.cu_rows + p.B);
+        if (HAS_INFO) {
+            griddep_wait();                 // row records of the prologue
+            bulk_g2s(&sh.info, reinterpret_cast<const RowInfo *>(p.ws_info) + r, 64u, &sh.mbar[0]);
+        } else {
             RowInfo inf = {};
             inf.b = r; inf.valid = 1;
             sh.info = inf;
         }
-        if (r < R) {
-            mbar_init(&sh.mbar[0], 1);
-            fence_mbar_init();
-            const uint32_t bytes = static_cast<uint32_t>(g.nb) * 16u;
-            mbar_arrive_expect_tx(&sh.mbar[0], bytes + (HAS_INFO ? 64u : 0u));
-            if (bytes) bulk_g2s(smem, row + g.a0, bytes, &sh.mbar[0]);
-            if (HAS_INFO) {
-                griddep_wait();                 // row records of the prologue
-                bulk_g2s(&sh.info, reinterpret_cast<const RowInfo *>(p.ws_info) + r, 64u, &sh.mbar[0]);
-            }
-        }
+        sh.R = min(R, p.R_cap);
     }
     float xe = -INFINITY;
     int32_t ie = INT_MAX;
-    if (tid < g.n_extra && r < p.R_cap) {
+    if (tid < g.n_extra) {
         ie = (tid < g.n_head) ? g.e0 + tid : g.a1 + (tid - g.n_head);
         xe = E::load(row, ie);
         sh.extras_v[tid] = xe;
         sh.extras_i[tid] = ie;
     }
     __syncthreads();
-    if (r >= sh.R) return;
-    if (tid == 0 && !mbar_wait(&sh.mbar[0], 0)) sh.timeout = 1;
+    if (tid == 0 && !mbar_wait(&sh.mbar[0], 0)) {
+        // the copy did not land in time: report it, give the copy one more
+        // bounded wait, and leave without touching the buffer
+        set_status(p.status, SPEC_STATUS_TIMEOUT);
+        mbar_wait(&sh.mbar[0], 0);
+        sh.timeout = 1;
+    }
     __syncthreads();
+    if (sh.timeout || r >= sh.R) return;
     const RowInfo &info = sh.info;
     if (!info.valid) return;
 
@@ -513,12 +629,13 @@ __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const Verify
     const float zd = info.zd;
     float tmax = -INFINITY, tsum = 0.f;
     int32_t targ = INT_MAX, tcnt = 0;
-    if (need_sum) tmax = pass1_sum<E, MODE>(body, g.nb, g.a0, zd, targ, tsum, tcnt);
-    else tmax = pass1_nosum<E, MODE>(body, g.nb, g.a0, zd, targ, tsum, tcnt);
+    if (need_sum) tmax = pass1<E, MODE, true>(body, g.nb, g.a0, zd, targ, tsum, tcnt);
+    else tmax = pass1<E, MODE, false>(body, g.nb, g.a0, zd, targ, tsum, tcnt);
     if (tid < g.n_extra)
         combine(tmax, targ, tsum, tcnt, xe, ie, 1.f, (MODE == MODE_RELAXED && xe > zd) ? 1 : 0,
                 need_sum);
     const float thread_max = tmax;
+    const int32_t thread_arg = targ;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float om = __shfl_xor_sync(0xFFFFFFFFu, tmax, o);
@@ -548,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const Verify
         if (lane == 0) {
             sh.part.m = m; sh.part.amax = a; sh.part.s = sm_; sh.part.cnt = cc;
             sh.part.gbest = -INFINITY; sh.part.gidx = INT_MAX; sh.part.ncand = 0;
-            sh.part.pad = 0;
+            sh.part.lev = -INFINITY;
         }
     }
     __syncthreads();
@@ -565,8 +682,7 @@ __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const Verify
         const bool unfiltered = !use_k && !use_m && !use_p;
         const bool pure_p = !use_k && !use_m && use_p;
         const float m_c = sh.part.m;
-        Cand *ws_list = reinterpret_cast<Cand *>(p.ws_cand) + rc * kCandCap;
-        float *ws_bins = p.ws_bins + rc * kBins;
+        const Noise nz{static_cast<uint32_t>(info.pos), info.rid, p.step, info.seed_lo, info.seed_hi};
         auto visit_chunk = [&](auto &&fn, float thr) {
             for (int i = tid; i < g.nb; i += kThreads) {
                 const uint4 v = body[i];
@@ -580,52 +696,53 @@ __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const Verify
             if (tid < g.n_extra && sh.extras_v[tid] >= thr) fn(sh.extras_v[tid], sh.extras_i[tid]);
         };
         if (!(m_c > -INFINITY)) {
-            if (pure_p && tid < kBins) ws_bins[tid] = 0.f;
-            if (pure_p && tid == 0) sh.part.gbest = 0.f;
+            // only -inf here: no candidates, no mass, no bins
+            if (pure_p && tid < kBins) p.ws_bins[rc * kBins + tid] = 0.f;
+            if (pure_p && tid == 0) { sh.part.gbest = 0.f; sh.part.gidx = INT_MIN + 1; }
         } else if (unfiltered) {
-            GumbelScorer gs{invT, static_cast<uint32_t>(info.pos), info.rid, p.step, info.seed_lo,
-                            info.seed_hi, 0xFFFFFFFFu, make_uint4(0, 0, 0, 0)};
+            // lower bound of the chunk's best score from the thread maxima;
+            // a vector whose max z has z/T + kGumbelMax below it cannot win
             float best = -INFINITY;
             int32_t bi = INT_MAX;
-            visit_chunk([&](float v, int32_t ix) {
-                const float sv = gs(v, ix);
-                if (sv > best || (sv == best && ix < bi)) { best = sv; bi = ix; }
-            }, -INFINITY);
+            if (thread_max > -INFINITY) { best = nz.score(thread_max, thread_arg, invT); bi = thread_arg; }
+            block_best(best, bi, sh);
+            const float skip = (best - kGumbelMax) * T;
+            const bool whole_blocks = (g.a0 & 3) == 0;
+            for (int i = tid; i < g.nb; i += kThreads) {
+                const uint4 v = body[i];
+                if (!(E::vmax(v) >= skip)) continue;
+                float x[VEC];
+                E::unpack(v, x);
+                const int32_t base = g.a0 + i * VEC;
+                if (whole_blocks) {
+                    score_vec<VEC>(x, base, invT, nz, best, bi);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) keep_best(nz.score(x[q], base + q, invT), base + q, best, bi);
+                }
+            }
+            if (tid < g.n_extra)
+                keep_best(nz.score(sh.extras_v[tid], sh.extras_i[tid], invT), sh.extras_i[tid], best, bi);
             block_best(best, bi, sh);
             if (tid == 0) { sh.part.gbest = best; sh.part.gidx = bi; }
-        } else if (pure_p) {
-            // mass exp((z - m_c)/T) per bin of T/8 below the chunk maximum;
-            // the last bin collects everything further down
-            for (int q = tid; q < kWarps * kBins; q += kThreads) wbins[q] = 0.f;
-            __syncthreads();
-            float wsum = 0.f;
-            const float bscale = kBinsPerT * invT;
-            float *mine = wbins + warp * kBins;
-            visit_chunk([&](float v, int32_t) {
-                const float d = m_c - v;
-                const float w = ex2(-d * sc);
-                wsum += w;
-                const float q = fminf(d * bscale, static_cast<float>(kBins - 1));
-                atomicAdd(mine + static_cast<int>(q), w);
-            }, -INFINITY);
-            wsum = block_sum(wsum, sh);
-            if (tid < kBins) {
-                float t = 0.f;
-                for (int w = 0; w < kWarps; ++w) t += wbins[w * kBins + tid];
-                ws_bins[tid] = t;
-            }
-            if (tid == 0) sh.part.gbest = wsum;
         } else {
-            // lower bound of the survivor threshold within this chunk:
-            // min-p relative to the chunk maximum (<= the row maximum); for
-            // top-k a ladder level holding k thread maxima
+            // level the candidates lie above: min-p relative to the chunk
+            // maximum (<= the row maximum); for top-k the exact k-th largest
+            // thread maximum (the ladder above the thread count); pure top-p
+            // keeps a short list used when it covers the nucleus boundary
             float lo = use_m ? m_c + T * logf(info.min_p) : -INFINITY;
             bool bounded = use_m;
-            if (use_k) {
-                float tlo = -INFINITY;
-                if (kth_level(thread_max, m_c, info.top_k, tlo, sh)) {
-                    lo = fmaxf(lo, tlo);
+            const int kk = use_k ? info.top_k : (pure_p ? kPureListK : 0);
+            if (kk > 0) {
+                if (kk <= kThreads) {
+                    lo = fmaxf(lo, kth_thread_max<E>(thread_max, kk, m_c, sh));
                     bounded = true;
+                } else {
+                    float tlo = -INFINITY;
+                    if (kth_level(thread_max, m_c, kk, tlo, sh)) {
+                        lo = fmaxf(lo, tlo);
+                        bounded = true;
+                    }
                 }
             }
             int n = INT_MAX;                     // unbounded: overflow marker
@@ -638,24 +755,59 @@ __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const Verify
                 }, lo);
                 __syncthreads();
                 n = sh.cand_n;
+                Cand *ws_list = reinterpret_cast<Cand *>(p.ws_cand) + rc * kCandCap;
                 for (int i = tid; i < min(n, kCandCap); i += kThreads) ws_list[i] = cand[i];
             }
-            if (tid == 0) sh.part.ncand = n;
+            if (tid == 0) { sh.part.ncand = n; sh.part.lev = lo; }
+            if (pure_p) {
+                // mass exp((z - m_c)/T) on the absolute grid; bin t (0 =
+                // the chunk max's bin) holds its elements' weights scaled by
+                // e^(t/8), which keeps each in (e^-1/8, e^1/8), as 2^20
+                // fixed point per warp (no float atomics); the rest of the
+                // mass is summed in registers
+                for (int q = tid; q < kWarps * kBins; q += kThreads) wbins[q] = 0u;
+                __syncthreads();
+                const float s8 = bin_scale(T);
+                const int32_t jt = abs_bin(m_c, s8);
+                uint32_t *mine = wbins + warp * kBins;
+                float tail = 0.f;
+                visit_chunk([&](float v, int32_t) {
+                    const int32_t t = jt - abs_bin(v, s8);
+                    if (t < kBins) {
+                        const float w = ex2(fmaf(v - m_c, invT, static_cast<float>(t) * (1.0f / kBinsPerT)) * kLog2e);
+                        atomicAdd(mine + t, __float2uint_rn(fminf(w, 1.25f) * kFix));
+                    } else {
+                        tail += ex2((v - m_c) * sc);
+                    }
+                }, -INFINITY);
+                __syncthreads();
+                float mass = 0.f;
+                if (tid < kBins) {
+                    uint64_t s = 0;
+                    for (int w = 0; w < kWarps; ++w) s += wbins[w * kBins + tid];
+                    mass = static_cast<float>(s) * (1.0f / kFix) *
+                           ex2(-static_cast<float>(tid) * (kLog2e / kBinsPerT));
+                    p.ws_bins[rc * kBins + tid] = mass;
+                }
+                const float Wc = block_sum(mass + tail, sh);
+                if (tid == 0) {
+                    sh.part.gbest = Wc;
+                    // grid origins beyond 2^21 lose the bin resolution
+                    sh.part.gidx = (jt > (1 << 21) || jt < -(1 << 21)) ? kNoBins : jt;
+                }
+            }
         }
         __syncthreads();
     }
-    if (tid == 0) {
-        reinterpret_cast<ChunkPart *>(p.ws_part)[rc] = sh.part;
-        if (sh.timeout) set_status(p.status, SPEC_STATUS_TIMEOUT);
-    }
+    if (tid == 0) reinterpret_cast<ChunkPart *>(p.ws_part)[rc] = sh.part;
 }
 
 // ------------------------------------------------------ finish kernel ----
 
 // Visit every element of a row with value >= thr as fn(value, index): the
 // aligned body streams through two shared-memory stages by TMA bulk copies
-// (phase bits in sh.ph), the unaligned head / tail use plain loads.  Called
-// by all threads of the CTA.
+// (phase bits in ph), the unaligned head / tail use plain loads.  Called by
+// all threads of the CTA.
 template <typename E, typename F>
 __device__ void visit_row(const void *row_v, int V, int h, uint8_t *stage_mem, Shared &sh,
                           uint32_t *ph, float thr, F &&fn)
@@ -709,13 +861,12 @@ template <typename TIn, int MODE>
 __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParams p)
 {
     using E = Elt<TIn>;
-    constexpr int VEC = E::VEC;
-    constexpr int PASSES = (sizeof(TIn) == 2) ? 2 : 4;
     extern __shared__ __align__(128) uint8_t smem[];
     Shared &sh = *reinterpret_cast<Shared *>(smem);
     ChunkPart *parts = reinterpret_cast<ChunkPart *>(smem + sizeof(Shared));       // [kMaxChunks]
     Cand *band = reinterpret_cast<Cand *>(parts + kMaxChunks);                     // [kBandCap]
     uint8_t *stage_mem = reinterpret_cast<uint8_t *>(band + kBandCap);             // 2 x kRowStage
+    Cand *lst = reinterpret_cast<Cand *>(stage_mem);                               // or [kListCap]
     __shared__ uint32_t ph[2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = blockIdx.x;
@@ -744,7 +895,7 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
         const float4 b = __ldcg(reinterpret_cast<const float4 *>(rp + tid) + 1);
         ChunkPart cp;
         cp.m = a.x; cp.amax = __float_as_int(a.y); cp.s = a.z; cp.cnt = __float_as_int(a.w);
-        cp.gbest = b.x; cp.gidx = __float_as_int(b.y); cp.ncand = __float_as_int(b.z); cp.pad = 0;
+        cp.gbest = b.x; cp.gidx = __float_as_int(b.y); cp.ncand = __float_as_int(b.z); cp.lev = b.w;
         parts[tid] = cp;
     }
     __syncthreads();
@@ -791,180 +942,219 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
         const bool use_p = info.top_p < 1.f;
         const bool unfiltered = !use_k && !use_m && !use_p;
         const bool pure_p = !use_k && !use_m && use_p;
-        GumbelScorer gs{invT, static_cast<uint32_t>(info.pos), info.rid, p.step, info.seed_lo,
-                        info.seed_hi, 0xFFFFFFFFu, make_uint4(0, 0, 0, 0)};
+        const uint32_t keyM = fkey(M);
+        GumbelScorer gs{invT, Noise{static_cast<uint32_t>(info.pos), info.rid, p.step, info.seed_lo,
+                                    info.seed_hi},
+                        0xFFFFFFFFu, make_uint4(0, 0, 0, 0)};
         float best = -INFINITY;
         int32_t bi = INT_MAX;
+        auto score_all = [&](float v, int32_t ix) { keep_best(gs(v, ix), ix, best, bi); };
+        auto visit_all = [&](auto &&fn, float thr) {
+            visit_row<E>(row, p.V, h, stage_mem, sh, ph, thr, fn);
+        };
         if (unfiltered) {
-            for (int q = tid; q < nchunk; q += kThreads) {
-                const float gb = parts[q].gbest;
-                const int32_t gi = parts[q].gidx;
-                if (gb > best || (gb == best && gi < bi)) { best = gb; bi = gi; }
-            }
-            block_best(best, bi, sh);
-        } else if (pure_p) {
-            // W from the chunk sums; bracket the nucleus boundary with the
-            // chunk bins: with levels L_k = k/8 (units of T below M),
-            //   LB(L) = mass of bins lying wholly within distance < L,
-            //   UB(L) = mass of bins starting at a distance < L;
-            // values at distance <= L_in (UB(L_in) < top_p W) are in the
-            // nucleus, values at distance >= L_out (LB(L_out) >= top_p W) are
-            // out; the band between is settled exactly.
-            float *cum = reinterpret_cast<float *>(band);           // [nchunk][kBins] prefix sums
-            const float *rb = p.ws_bins + static_cast<int64_t>(r) * nchunk * kBins;
-            for (int q = tid; q < nchunk * kBins; q += kThreads) cum[q] = __ldcg(rb + q);
-            __syncthreads();
-            for (int q = tid; q < nchunk; q += kThreads) {
-                float run = 0.f;
-                for (int j = 0; j < kBins; ++j) { run += cum[q * kBins + j]; cum[q * kBins + j] = run; }
-            }
-            if (tid == 0) {
-                float w = 0.f;
-                for (int q = 0; q < nchunk; ++q)
-                    if (parts[q].m > -INFINITY) w += parts[q].gbest * ex2((parts[q].m - M) * sc);
-                sh.W = w;
-            }
-            __syncthreads();
-            const float W = sh.W, target = info.top_p * W;
-            // thread t evaluates level L = t / kBinsPerT (t = 0..255)
-            const float L = static_cast<float>(tid) / kBinsPerT;
-            float lb = 0.f, ub = 0.f;
-            for (int q = 0; q < nchunk; ++q) {
-                const float mq = parts[q].m;
-                if (!(mq > -INFINITY)) continue;
-                const float delta = (M - mq) * invT;
-                const float fac = ex2((mq - M) * sc);
-                // bins j < kBins-1 cover [delta + j/8, delta + (j+1)/8); the last
-                // bin covers [delta + (kBins-1)/8, inf)
-                const float u = (L - delta) * kBinsPerT;
-                const int j_lb = static_cast<int>(fminf(floorf(u), static_cast<float>(kBins - 1))) - 1;
-                const int j_ub = static_cast<int>(fminf(ceilf(u), static_cast<float>(kBins))) - 1;
-                if (j_lb >= 0) lb += cum[q * kBins + j_lb] * fac;
-                if (j_ub >= 0) ub += cum[q * kBins + min(j_ub, kBins - 1)] * fac;
-            }
-            int *flags = reinterpret_cast<int *>(sh.hist);
-            flags[tid] = (ub < target ? 1 : 0) | (lb >= target ? 2 : 0);
-            __syncthreads();
-            if (tid == 0) {
-                int kin = -1, kout = -1;
-                for (int t = 0; t < kThreads; ++t) {
-                    if (flags[t] & 1) kin = t;
-                    if ((flags[t] & 2) && kout < 0) kout = t;
-                }
-                sh.band_lo = kin;
-                sh.band_hi = kout;
-            }
-            __syncthreads();
-            const float eps = 1e-3f;
-            const float din = (sh.band_lo < 0) ? -1.f : static_cast<float>(sh.band_lo) / kBinsPerT - eps;
-            const float dout = (sh.band_hi < 0) ? INFINITY : static_cast<float>(sh.band_hi) / kBinsPerT + eps;
-            // one pass over the row: Gumbel-max over the sure part, exact mass
-            // of the sure part, the band collected on chip
-            if (tid == 0) sh.cand_n = 0;
-            __syncthreads();
-            float mass_in = 0.f;
-            const float thr = (dout == INFINITY) ? -INFINITY : M - dout * T;
-            visit_row<E>(row, p.V, h, stage_mem, sh, ph, thr, [&](float v, int32_t ix) {
-                const float d = (M - v) * invT;
-                if (d <= din) {
-                    mass_in += ex2((v - M) * sc);
-                    const float sv = gs(v, ix);
-                    if (sv > best || (sv == best && ix < bi)) { best = sv; bi = ix; }
-                } else if (d < dout) {
-                    const int slot = atomicAdd(&sh.cand_n, 1);
-                    if (slot < kBandCap) { band[slot].v = v; band[slot].i = ix; }
-                }
-            });
-            mass_in = block_sum(mass_in, sh);
-            const int nband = sh.cand_n;
-            if (nband <= kBandCap) {
-                if (nband > 0) {
-                    auto visit_band = [&](auto &&fn, float t2) {
-                        for (int i = tid; i < nband; i += kThreads)
-                            if (band[i].v >= t2) fn(band[i].v, band[i].i);
-                    };
-                    const float tgt = target - mass_in;
-                    uint32_t kF = 0u;
-                    if (tgt > 0.f) kF = radix_select<true>(visit_band, 0u, tgt, 0u, M, sc, PASSES, sh);
-                    else kF = 0xFFFFFFFFu;           // the sure part already holds the mass
-                    visit_band([&](float v, int32_t ix) {
-                        if (fkey(v) < kF) return;
-                        const float sv = gs(v, ix);
-                        if (sv > best || (sv == best && ix < bi)) { best = sv; bi = ix; }
-                    }, -INFINITY);
-                }
-            } else {
-                // band too large: exact mass select over the whole row
-                best = -INFINITY;
-                bi = INT_MAX;
-                auto visit_all = [&](auto &&fn, float t2) {
-                    visit_row<E>(row, p.V, h, stage_mem, sh, ph, t2, fn);
-                };
-                const uint32_t kF = radix_select<true>(visit_all, 0u, target, 0u, M, sc, PASSES, sh);
-                visit_all([&](float v, int32_t ix) {
-                    if (fkey(v) < kF) return;
-                    const float sv = gs(v, ix);
-                    if (sv > best || (sv == best && ix < bi)) { best = sv; bi = ix; }
-                }, key_floor(kF));
-            }
+            for (int q = tid; q < nchunk; q += kThreads) keep_best(parts[q].gbest, parts[q].gidx, best, bi);
             block_best(best, bi, sh);
         } else {
-            // top-k and / or min-p: candidates from the chunk lists, or from
-            // the row itself when a list overflowed
-            const float th_m = use_m ? M + T * logf(info.min_p) : -INFINITY;
+            // candidate lists: offsets, overflow, the lowest and highest
+            // levels they lie above
             if (tid == 0) {
                 int tot = 0, ovf = 0;
+                float th = -INFINITY, lmin = INFINITY;
                 for (int q = 0; q < nchunk; ++q) {
+                    sh.offs[q] = tot;
+                    if (!(parts[q].m > -INFINITY)) continue;
                     const int nq = parts[q].ncand;
                     ovf |= (nq > kCandCap);
                     tot += min(nq, kCandCap);
+                    th = fmaxf(th, parts[q].lev);
+                    lmin = fminf(lmin, parts[q].lev);
                 }
+                sh.offs[nchunk] = tot;
                 sh.total = tot;
                 sh.overflow = ovf;
+                sh.theta = th;
+                sh.lkey = (lmin == INFINITY) ? 0u : fkey(lmin);
             }
             __syncthreads();
-            const bool whole = sh.overflow != 0;
             const int n_list = sh.total;
-            auto visit = [&](auto &&fn, float thr) {
-                if (whole) {
-                    visit_row<E>(row, p.V, h, stage_mem, sh, ph, thr, fn);
-                } else {
-                    int base = 0;
-                    for (int q = 0; q < nchunk; ++q) {
-                        const int nq = min(parts[q].ncand, kCandCap);
-                        const float2 *lq = reinterpret_cast<const float2 *>(p.ws_cand) +
-                                           (static_cast<int64_t>(r) * nchunk + q) * kCandCap;
-                        for (int i = ((tid - base) % kThreads + kThreads) % kThreads; i < nq; i += kThreads) {
-                            const float2 e = __ldcg(lq + i);
-                            if (e.x >= thr) fn(e.x, __float_as_int(e.y));
-                        }
-                        base += nq;
+            const bool staged = !sh.overflow && n_list <= kListCap;
+            auto stage_lists = [&]() {
+                const float2 *wl = reinterpret_cast<const float2 *>(p.ws_cand) +
+                                   static_cast<int64_t>(r) * nchunk * kCandCap;
+                for (int e = tid; e < n_list; e += kThreads) {
+                    int q = 0;
+                    while (sh.offs[q + 1] <= e) ++q;
+                    const float2 v = __ldcg(wl + static_cast<int64_t>(q) * kCandCap + (e - sh.offs[q]));
+                    lst[e].v = v.x;
+                    lst[e].i = __float_as_int(v.y);
+                }
+                __syncthreads();
+            };
+            auto visit_lst = [&](auto &&fn, float thr) {
+                for (int i = tid; i < n_list; i += kThreads) {
+                    const Cand e = lst[i];
+                    if (e.v >= thr) fn(e.v, e.i);
+                }
+            };
+            // lists in global memory (more than fit on chip)
+            auto visit_gl = [&](auto &&fn, float thr) {
+                for (int q = 0; q < nchunk; ++q) {
+                    if (!(parts[q].m > -INFINITY)) continue;
+                    const int nq = min(parts[q].ncand, kCandCap);
+                    const float2 *lq = reinterpret_cast<const float2 *>(p.ws_cand) +
+                                       (static_cast<int64_t>(r) * nchunk + q) * kCandCap;
+                    for (int i = tid; i < nq; i += kThreads) {
+                        const float2 e = __ldcg(lq + i);
+                        if (e.x >= thr) fn(e.x, __float_as_int(e.y));
                     }
                 }
             };
-            uint32_t key_S = use_m ? fkey(th_m) : 0u;
-            if (use_k && (whole || n_list >= info.top_k))
-                key_S = max(key_S, radix_select<false>(visit, key_S, 0.f,
-                                                       static_cast<uint32_t>(info.top_k), M, sc,
-                                                       PASSES, sh));
-            uint32_t key_F = key_S;
-            if (use_p) {
-                float w = 0.f;
-                const uint32_t kS = key_S;
-                visit([&](float v, int32_t) {
-                    if (fkey(v) >= kS) w += ex2((v - M) * sc);
-                }, key_floor(key_S));
-                const float W = block_sum(w, sh);
-                key_F = max(key_S, radix_select<true>(visit, key_S, info.top_p * W, 0u, M, sc,
-                                                      PASSES, sh));
+            if (pure_p) {
+                // ---- top-p alone: bracket the boundary with the bins ----
+                const float s8 = bin_scale(T);
+                if (tid == 0) {
+                    float w = 0.f;
+                    int32_t J = INT_MIN, nob = 0;
+                    for (int q = 0; q < nchunk; ++q) {
+                        if (!(parts[q].m > -INFINITY)) continue;
+                        w += parts[q].gbest * ex2((parts[q].m - M) * sc);
+                        nob |= (parts[q].gidx == kNoBins);
+                        J = max(J, parts[q].gidx);
+                    }
+                    sh.W = w;
+                    sh.J = J;
+                    sh.nobins = nob;
+                }
+                __syncthreads();
+                const float target = info.top_p * sh.W;
+                const int32_t J = sh.J;
+                bool whole = sh.nobins != 0;
+                int32_t qin = 0, qband = 0;
+                if (!whole) {
+                    // combined mass of absolute bin J - t, then C(t) = mass of
+                    // bins J - t .. J (thread t)
+                    float hb = 0.f;
+                    if (tid < kBins) {
+                        const float *rb = p.ws_bins + static_cast<int64_t>(r) * nchunk * kBins;
+                        for (int q = 0; q < nchunk; ++q) {
+                            if (!(parts[q].m > -INFINITY)) continue;
+                            const int tq = tid - (J - parts[q].gidx);
+                            if (tq >= 0 && tq < kBins)
+                                hb += __ldcg(rb + q * kBins + tq) * ex2((parts[q].m - M) * sc);
+                        }
+                    }
+                    float cum = hb;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float n = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+                        if (lane >= o) cum += n;
+                    }
+                    float *wt = reinterpret_cast<float *>(sh.scan);
+                    if (lane == 31) wt[warp] = cum;
+                    __syncthreads();
+                    for (int w = 0; w < warp; ++w) cum += wt[w];
+                    // bins 0..a are surely inside (mass above < target), bins
+                    // from b on surely outside; the band between is settled
+                    // exactly below
+                    const int n_in = __syncthreads_count(tid < kBins && cum < target * (1.f - kMassTol));
+                    const int n_out = __syncthreads_count(tid < kBins && cum >= target * (1.f + kMassTol));
+                    const int a = n_in - 1, b = kBins - n_out;
+                    if (b >= kBins) whole = true;       // the nucleus reaches below the bins
+                    qin = J - a;
+                    qband = J - b;
+                }
+                if (!whole) {
+                    // the lists cover the band when every value below the
+                    // highest list level falls in a bin below the band
+                    const bool from_lists = staged && abs_bin(sh.theta, s8) < qband;
+                    if (from_lists) stage_lists();
+                    if (tid == 0) sh.cand_n = 0;
+                    __syncthreads();
+                    float mass_in = 0.f;
+                    auto classify = [&](float v, int32_t ix) {
+                        const int32_t qz = abs_bin(v, s8);
+                        if (qz >= qin) {
+                            mass_in += ex2((v - M) * sc);
+                            score_all(v, ix);
+                        } else if (qz >= qband) {
+                            const int slot = atomicAdd(&sh.cand_n, 1);
+                            if (slot < kBandCap) { band[slot].v = v; band[slot].i = ix; }
+                        }
+                    };
+                    // values below thr lie in bins below the band
+                    const float thr = (J > (1 << 21) || J < -(1 << 21))
+                                          ? -INFINITY
+                                          : static_cast<float>(qband - 1) / s8;
+                    if (from_lists) visit_lst(classify, thr);
+                    else visit_all(classify, thr);
+                    mass_in = block_sum(mass_in, sh);
+                    const int nband = sh.cand_n;
+                    const float tgt = target - mass_in;
+                    if (nband > kBandCap) {
+                        whole = true;
+                    } else if (nband > 0 && tgt > 0.f) {
+                        uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
+                        for (int i = tid; i < nband; i += kThreads) {
+                            const uint32_t k = fkey(band[i].v);
+                            kmn = min(kmn, k);
+                            kmx = max(kmx, k);
+                        }
+                        block_minmax(kmn, kmx, sh);
+                        auto visit_band = [&](auto &&fn, float t2) {
+                            for (int i = tid; i < nband; i += kThreads)
+                                if (band[i].v >= t2) fn(band[i].v, band[i].i);
+                        };
+                        const uint32_t kF = select_key<E, true>(visit_band, kmn, kmx, tgt, 0u, M, sc, sh);
+                        visit_band([&](float v, int32_t ix) {
+                            if (fkey(v) >= kF) score_all(v, ix);
+                        }, -INFINITY);
+                    }
+                }
+                if (whole) {
+                    // exact mass select over the whole row
+                    best = -INFINITY;
+                    bi = INT_MAX;
+                    const uint32_t kF = select_key<E, true>(visit_all, 0u, keyM, target, 0u, M, sc, sh);
+                    visit_all([&](float v, int32_t ix) {
+                        if (fkey(v) >= kF) score_all(v, ix);
+                    }, key_floor(kF));
+                }
+                block_best(best, bi, sh);
+            } else {
+                // ---- top-k and / or min-p (then top-p over the survivors) --
+                const bool whole = sh.overflow != 0;
+                if (staged) stage_lists();
+                auto visit = [&](auto &&fn, float thr) {
+                    if (whole) visit_all(fn, thr);
+                    else if (staged) visit_lst(fn, thr);
+                    else visit_gl(fn, thr);
+                };
+                const float th_m = use_m ? M + T * logf(info.min_p) : -INFINITY;
+                uint32_t key_S = use_m ? fkey(th_m) : 0u;
+                // every list element lies above its chunk's level
+                const uint32_t lo_k = whole ? key_S : max(key_S, sh.lkey);
+                if (use_k && (whole || n_list >= info.top_k))
+                    key_S = max(key_S, select_key<E, false>(visit, lo_k, keyM, 0.f,
+                                                            static_cast<uint32_t>(info.top_k), M,
+                                                            sc, sh));
+                uint32_t key_F = key_S;
+                if (use_p) {
+                    float w = 0.f;
+                    const uint32_t kS = key_S;
+                    visit([&](float v, int32_t) {
+                        if (fkey(v) >= kS) w += ex2((v - M) * sc);
+                    }, key_floor(key_S));
+                    const float Wt = block_sum(w, sh);
+                    key_F = max(key_S, select_key<E, true>(visit, key_S, keyM, info.top_p * Wt, 0u,
+                                                           M, sc, sh));
+                }
+                const uint32_t kF = key_F;
+                visit([&](float v, int32_t ix) {
+                    if (fkey(v) >= kF) score_all(v, ix);
+                }, key_floor(key_F));
+                block_best(best, bi, sh);
             }
-            const uint32_t kF = key_F;
-            visit([&](float v, int32_t ix) {
-                if (fkey(v) < kF) return;
-                const float sv = gs(v, ix);
-                if (sv > best || (sv == best && ix < bi)) { best = sv; bi = ix; }
-            }, key_floor(key_F));
-            block_best(best, bi, sh);
         }
         y = (bi == INT_MAX) ? AMAX : bi;
     }

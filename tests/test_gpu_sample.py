@@ -44,14 +44,16 @@ def test_stochastic_full_size_workload():
 @pytest.mark.parametrize("T,k,tp,mp", [
     (1.0, 0, 1.0, 0.0),      # no filter: Gumbel over the whole vocabulary
     (0.5, 0, 1.0, 0.0),
-    (1.0, 0, 0.9, 0.0),      # pure top-p (cluster-wide selects)
+    (1.0, 0, 0.9, 0.0),      # pure top-p (bin bracket, band settled exactly)
     (0.5, 0, 0.9, 0.0),
     (0.7, 0, 0.5, 0.0),
-    (1.0, 20, 1.0, 0.0),     # top-k with warp-maximum bound
+    (1.0, 20, 1.0, 0.0),     # top-k: chunk lists above the k-th thread maximum
     (1.0, 50, 0.9, 0.05),
     (0.5, 0, 1.0, 0.05),     # min-p only
     (1.0, 0, 0.95, 0.05),
-    (1.0, 200, 1.0, 0.0),    # top-k beyond the warp-maximum bound (cluster-wide)
+    (1.0, 200, 1.0, 0.0),
+    (1.0, 256, 1.0, 0.0),    # the largest k bounded by the thread maxima
+    (1.0, 257, 1.0, 0.0),    # beyond it: ladder bound, else the whole row
     (1.0, 1000, 0.8, 0.0),
     (2.0, 5, 1.0, 1e-6),
     (1.0, 1, 1.0, 0.0),      # top-k = 1: the maximum tie group
@@ -78,7 +80,7 @@ def test_small_and_unaligned_rows(V, ld):
 
 def test_flat_rows_overflow_candidates():
     """Many exact ties at the top (integer logits): candidate lists overflow
-    and the cluster-wide path takes over."""
+    and the exact selects over the whole row take over."""
     sv = need_gpu()
     rng = np.random.default_rng(1)
     vb = W.ragged_batch(seed=2, B=4, k_max=3, V=152064, dtype="bf16")
@@ -151,3 +153,43 @@ def test_sampler_frequencies_match_filtered_distribution():
     n = B * steps
     assert counts[~F].sum() == 0
     assert scipy.stats.chisquare(counts[F], n * pF[F]).pvalue > 1e-4
+
+
+def shifted(vb, shift):
+    """Add a constant to every logit (re-rounded to the batch's dtype)."""
+    if shift == 0.0:
+        return vb
+    if vb.dtype == "bf16":
+        vb.logits = W.bf16_bits(W.bf16_bits_to_f32(vb.logits) + np.float32(shift))
+    else:
+        vb.logits = (vb.logits + np.float32(shift)).astype(np.float32)
+    return vb
+
+
+@pytest.mark.parametrize("T,tp,sigma,shift", [
+    (0.5, 0.9, 3.0, 0.0),     # small nucleus: settled from the candidate lists
+    (1.0, 0.9, 3.0, 0.0),     # diffuse nucleus: band from one pass over the row
+    (2.0, 0.7, 3.0, 0.0),
+    (1.0, 0.9, 0.3, 0.0),     # nearly flat rows: the band overflows, exact row selects
+    (1e-6, 0.9, 3.0, 20.0),   # grid origin beyond 2^21: exact row selects
+    (1.0, 0.99, 3.0, -40.0),  # all logits negative
+    (0.25, 0.5, 8.0, 0.0),    # nucleus of one or two values
+])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_pure_top_p_paths(T, tp, sigma, shift, dtype):
+    sv = need_gpu()
+    V = 152064 if dtype == "bf16" else 60000
+    vb = W.ragged_batch(seed=int(T * 100) + int(sigma * 10), B=6, k_max=3, V=V, dtype=dtype,
+                        sigma=sigma)
+    check(sv, shifted(vb, shift), params(vb.B, T, 0, tp, 0.0, seed=7))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_unfiltered_rows_not_block_aligned(dtype):
+    """Rows whose aligned body does not start on a Philox block (odd leading
+    dimension): per-element noise instead of whole-vector blocks."""
+    sv = need_gpu()
+    V = 152064 if dtype == "bf16" else 60000
+    vb = W.ragged_batch(seed=41, B=5, k_max=3, V=V, dtype=dtype, ld=V + 3)
+    for T in (0.5, 1.0):
+        check(sv, vb, params(vb.B, T, 0, 1.0, 0.0, seed=3))
