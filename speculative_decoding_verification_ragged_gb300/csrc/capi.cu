@@ -30,17 +30,19 @@ struct WsLayout {
     uint32_t *ticket, *rticket;
     void *info, *part, *cand;
     float *bins;
+    int32_t *hrows;
 };
 
 // tok [R_cap] | flag [R_cap] | ticket [B] | rticket [R_cap] | info [R_cap * 64 B] |
-// part [R_cap * nchunk * 32 B] | bins, cand (sampler only); 256-byte aligned
+// part [R_cap * nchunk * 32 B] | bins, cand, hrows (sampler only); 256-byte aligned
 size_t ws_bytes(int32_t R_cap, int32_t B, int32_t V, int elt, bool sampling)
 {
     const size_t R = static_cast<size_t>(R_cap);
     const size_t rc = R * static_cast<size_t>(chunks_per_row(V, elt));
     size_t n = 3 * align256(R * 4) + align256(static_cast<size_t>(B) * 4) + align256(R * 64) +
                align256(rc * 32);
-    if (sampling) n += align256(rc * kWsBins * 4) + align256(rc * kWsCandCap * 8);
+    if (sampling)
+        n += align256(rc * kWsBins * 4) + align256(rc * kWsCandCap * 8) + align256((R + 1) * 4);
     return n;
 }
 
@@ -66,6 +68,8 @@ WsLayout ws_layout(void *ws, int32_t R_cap, int32_t B, int32_t V, int elt, bool 
         l.bins = reinterpret_cast<float *>(p);
         p += align256(rc * kWsBins * 4);
         l.cand = p;
+        p += align256(rc * kWsCandCap * 8);
+        l.hrows = reinterpret_cast<int32_t *>(p);
     }
     return l;
 }
@@ -83,6 +87,10 @@ int check_batch(const spec_batch *b, const spec_outputs *o)
     if (reinterpret_cast<uintptr_t>(b->logits) % elt_bytes(b->dtype)) return SPEC_ERR_INVALID_ARG;
     if (static_cast<size_t>(b->V) * elt_bytes(b->dtype) > max_row_bytes()) return SPEC_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(b->R_cap) * b->ld > (int64_t(1) << 40)) return SPEC_ERR_UNSUPPORTED;
+    // one CTA per (row, chunk): the grid stays below 2^31
+    if (static_cast<int64_t>(b->R_cap) * chunks_per_row(b->V, static_cast<int>(elt_bytes(b->dtype))) >
+        INT32_MAX)
+        return SPEC_ERR_UNSUPPORTED;
     if ((o->acc == nullptr) != (o->ver == nullptr)) return SPEC_ERR_INVALID_ARG;
     return SPEC_OK;
 }
@@ -120,6 +128,7 @@ VerifyParams base_params(const spec_batch *b, const spec_outputs *o, void *ws, b
     p.ws_part = l.part;
     p.ws_bins = l.bins;
     p.ws_cand = l.cand;
+    p.ws_hrows = l.hrows;
     p.nchunk = chunks_per_row(b->V, elt);
     p.n_rows = b->R_cap;
     return p;
@@ -218,6 +227,8 @@ int spec_draft_confidence(const spec_draft *d, const spec_allocation *o, void *w
     const int64_t Q = static_cast<int64_t>(d->B) * d->k;
     if (Q * 4 + (static_cast<int64_t>(d->B) * 4 + 1) * 4 > 200 * 1024) return SPEC_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(Q) * d->ld > (int64_t(1) << 40)) return SPEC_ERR_UNSUPPORTED;
+    if (Q * chunks_per_row(d->V, static_cast<int>(elt_bytes(d->dtype))) > INT32_MAX)
+        return SPEC_ERR_UNSUPPORTED;
 
     const int elt = static_cast<int>(elt_bytes(d->dtype));
     if (!workspace || workspace_bytes < ws_bytes(static_cast<int32_t>(Q), 1, d->V, elt, false))

@@ -15,6 +15,7 @@ enum Mode : int { MODE_GREEDY = 0, MODE_RELAXED = 1, MODE_SAMPLE = 2, MODE_CONF 
 //   part[r][c]  (32 bytes) chunk reduction and sampler summary
 //   bins[r][c]  (kWsBins floats) pure top-p mass bins         (sampler only)
 //   cand[r][c]  (kWsCandCap (value, index) pairs) candidates  (sampler only)
+//   hrows       (1 + R_cap int32) rows queued for a second pass (sampler only)
 constexpr int kWsCandCap = 512;
 constexpr int kWsBins = 128;
 
@@ -62,6 +63,7 @@ struct VerifyParams {
     void *ws_part;               // [R_cap * nchunk] chunk partials (32 bytes each)
     float *ws_bins;              // [R_cap * nchunk * kWsBins]
     void *ws_cand;               // [R_cap * nchunk * kWsCandCap] (value, index) pairs
+    int32_t *ws_hrows;           // [1 + R_cap] rows queued for a second pass (count first)
     int32_t nchunk;              // chunks per row
     int32_t n_rows;              // rows of the grid
 };

@@ -2,20 +2,22 @@
 // greedy and relaxed top-K acceptance, the filtered Gumbel-max sampler with
 // the point-mass rejection chain, and the draft confidence.
 //
-// Three kernels per call, chained with programmatic dependent launch:
+// Kernels per call, chained with programmatic dependent launch:
 //
 //   prologue, one warp per packed row: the owner request (32-way search of
 //     cu_rows), the row's position and validity and the owner's parameters,
 //     as a 64-byte row record; requests without a valid row range get their
 //     outputs here.
-//   stream, one CTA per (row, chunk of kChunkBytes): thread 0 first issues
-//     one 1-D TMA bulk copy of the chunk's 16-byte-aligned body into shared
-//     memory, then a second one of the row record on the same mbarrier (the
-//     row is read from HBM exactly once; unaligned head/tail elements use
-//     plain loads).  Pass 1 runs a per-thread online max / first argmax /
-//     sum exp(z - max) over 16-byte vectors, plus the count of logits above
-//     the draft's logit for relaxed top-K; warp shuffles and a CTA reduction
-//     give the chunk summary.  For the sampler (T > 0):
+//   stream, one CTA per (row, chunk of kChunkBytes): thread 0 issues one 1-D
+//     TMA bulk copy of the chunk's 16-byte-aligned body into shared memory
+//     first, then one of the row record on the same mbarrier once the
+//     prologue has finished (the row is read from HBM exactly once;
+//     unaligned head/tail elements use plain loads); many short CTAs per SM
+//     keep the copies in flight.  Pass 1 runs a per-thread online max /
+//     first argmax / sum exp(z - max) over 16-byte vectors (packed f32x2
+//     arithmetic for bf16), plus the count of logits above the draft's logit
+//     for relaxed top-K; warp shuffles and a CTA reduction give the chunk
+//     summary.  For the sampler (T > 0):
 //       no filter   - the chunk's own Gumbel-max winner (vectors that cannot
 //                     beat a lower bound taken from the thread maxima are
 //                     skipped);
@@ -34,13 +36,19 @@
 //     sampler run radix selects (exact k-th largest value, exact top-p mass
 //     crossing) over the candidate lists staged in shared memory and
 //     Gumbel-max over the survivors with Philox4x32-10 uniforms.  Pure top-p
-//     brackets the nucleus boundary with the combined bins and settles it
-//     exactly on the one band of bins the bracket cannot decide, from the
-//     candidate lists when they cover the band, else from one pass over the
-//     row streamed through shared memory by TMA.  The CTA finishing the last
-//     row of a request (atomic ticket) runs the accept-while-equal prefix
-//     scan with one warp ballot and writes the request's tokens and the
-//     optional prefix-acceptance counters.
+//     brackets the nucleus boundary with the combined bins; when the lists
+//     cover the undecided band the row is settled from them.  A row that
+//     needs its logits again (a nucleus wider than the lists, or a list or
+//     band overflow) is queued for the heavy kernel with a short record.
+//     The CTA finishing the last row of a request (atomic ticket) runs the
+//     accept-while-equal prefix scan with one warp ballot and writes the
+//     request's tokens and the optional prefix-acceptance counters.
+//   heavy (sampler only), persistent over the queued rows' chunks: each
+//     chunk is staged by TMA, its nucleus and band values are compacted in
+//     shared memory and the nucleus scored with all lanes busy, its band
+//     values go to a per-chunk list; the CTA finishing a row's last chunk
+//     (atomic ticket) settles the band exactly, or runs exact selects over
+//     the whole row when a band or list overflowed, then runs the chain.
 //
 // Definitions: xLLM docs "自适应投机推理" §"启动示例" (ragged rejection
 // sampler with packed-row owners, point-mass draft, replacement / bonus,
@@ -63,9 +71,10 @@ constexpr int kBins = kWsBins;          // pure top-p mass bins per chunk
 constexpr float kBinsPerT = 8.0f;       // bin width T/8
 constexpr float kFix = 1048576.0f;      // fixed-point scale of one bin weight (2^20)
 constexpr int32_t kNoBins = INT_MIN;    // chunk grid origin too large for exact bins
-constexpr int kBandCap = 2048;          // undecided values the finish kernel keeps on chip
+constexpr int kBandCap = 2048;          // undecided values kept on chip
 constexpr int kListCap = 2048;          // candidates the finish kernel stages on chip
-constexpr int kRowStage = 16 * 1024;    // finish kernel: bytes per row-streaming stage
+constexpr int kSureCap = 2048;          // heavy kernel: nucleus values compacted per chunk
+constexpr int kRowStage = 16 * 1024;    // heavy kernel: bytes per row-streaming stage
 constexpr int kPureListK = 64;          // pure top-p: list above the 64-th thread maximum
 constexpr float kMassTol = 1e-5f;       // relative slack of the bin bracket
 // Largest Gumbel noise of the uniform lattice: u <= 1 - 2^-24 gives
@@ -93,9 +102,28 @@ struct __align__(16) ChunkPart {
     float lev;      // sampler with a bound: the level the candidates lie above
 };
 static_assert(sizeof(ChunkPart) == 32, "chunk summary is 32 bytes");
-static_assert(kListCap * 8 <= 2 * kRowStage, "lists fit in the row stages");
+static_assert(2 * kRowStage <= kChunkBytes, "the heavy kernel streams rows through its chunk buffer");
 
-// shared scratch common to both row kernels
+// Record of a row queued for the heavy kernel (32 bytes, at the start of the
+// row's bin area, whose bins are no longer needed).
+constexpr int32_t kHeavyBand = 1;       // settle the band over the chunks
+constexpr int32_t kHeavyWhole = 2;      // exact selects over the whole row
+struct __align__(16) HeavyRec {
+    int32_t mode, qin, qband, amax;
+    float M, target;
+    float zin, zband;   // the same classes as value thresholds: abs_bin(z) >= q iff z >= zq
+};
+static_assert(sizeof(HeavyRec) == 32, "heavy record is 32 bytes");
+
+// per-chunk result of the heavy pass (16 bytes, after the record)
+struct __align__(16) HeavyPart {
+    float best;     // best Gumbel score among the chunk's nucleus values
+    int32_t bi;     //   and its index
+    float mass;     // their mass exp((z - M)/T)
+    int32_t nband;  // band values stored in the chunk's list (> kCandCap: overflow)
+};
+
+// shared scratch common to the row kernels
 struct __align__(16) Shared {
     RowInfo info;
     ChunkPart part;
@@ -105,7 +133,7 @@ struct __align__(16) Shared {
     int32_t red_i[kWarps * 2];
     int32_t offs[kMaxChunks + 1];
     float M, S, W, sel_excl_f, theta;
-    int32_t AMAX, CNT, sel_bin, sel_found, total, overflow, cand_n, R, J, nobins;
+    int32_t AMAX, CNT, sel_bin, sel_found, total, overflow, cand_n, R, J, nobins, last, heavy;
     uint32_t sel_excl_u, lkey;
     float extras_v[16];
     int32_t extras_i[16];
@@ -190,7 +218,9 @@ __device__ __forceinline__ float key_floor(uint32_t k)
 // (fn(v, i) for every element >= thr).  Values are compared through their
 // order-preserving keys; bf16 values have 16 significant key bits, fp32 32.
 // Only keys in [lo, hi] take part (hi must bound every such key from above).
-// Digits of 8 bits start at the highest bit where lo and hi differ.
+// The first digit holds the 8 bits below and including the highest bit where
+// lo and hi differ (the bits above are common), so it spreads the values
+// over the bins; later digits take the next 8 bits (the last one fewer).
 //   COUNT (MASS = false): the key of the k-th largest value.
 //   MASS: the key of the value group where the cumulative weight
 //     exp((z - M) * sc), counted from the top, first reaches `target`.
@@ -203,21 +233,24 @@ __device__ uint32_t select_key(Visit &&visit, uint32_t lo, uint32_t hi, float ta
     constexpr int VS = (E::BYTES == 2) ? 16 : 0;
     const uint32_t vlo = lo >> VS, vhi = hi >> VS;
     const uint32_t x = vlo ^ vhi;
-    int shift = x ? ((31 - __clz(x)) / 8) * 8 : 0;
-    uint32_t prefix = (shift + 8 >= 32) ? 0u : (vhi >> (shift + 8));
+    const int top = x ? 31 - __clz(x) : 0;
+    int shift = max(top - 7, 0);
+    int width = top - shift + 1;
+    uint32_t prefix = (top + 1 >= 32) ? 0u : (vhi >> (top + 1));
     const float thr = key_floor(lo);
     const int t = threadIdx.x;
     for (;;) {
         sh.hist[t] = 0u;
         __syncthreads();
-        const int sh8 = shift + 8;
+        const int above = shift + width;
+        const uint32_t dmask = (1u << width) - 1u;
         const bool wide = MASS && shift > 0;
         visit([&](float v, int32_t) {
             const uint32_t fk = fkey(v);
             if (fk < lo) return;
             const uint32_t vk = fk >> VS;
-            if (sh8 < 32 && (vk >> sh8) != prefix) return;
-            const uint32_t bin = (vk >> shift) & 255u;
+            if (above < 32 && (vk >> above) != prefix) return;
+            const uint32_t bin = (vk >> shift) & dmask;
             if (wide) atomicAdd(reinterpret_cast<float *>(&sh.hist[bin]), ex2((v - M) * sc));
             else atomicAdd(&sh.hist[bin], 1u);
         }, thr);
@@ -227,7 +260,7 @@ __device__ uint32_t select_key(Visit &&visit, uint32_t lo, uint32_t hi, float ta
             const uint32_t c = sh.hist[t];
             float w = 0.f;
             if (c) {
-                const uint32_t vk = (prefix << 8) | static_cast<uint32_t>(t);
+                const uint32_t vk = (prefix << width) | static_cast<uint32_t>(t);
                 const uint32_t fk = VS ? ((vk << 16) | ((vk & 0x8000u) ? 0u : 0xFFFFu)) : vk;
                 w = static_cast<float>(c) * ex2((key_value(fk) - M) * sc);
             }
@@ -240,13 +273,27 @@ __device__ uint32_t select_key(Visit &&visit, uint32_t lo, uint32_t hi, float ta
         const int bin = sh.sel_bin;
         if (MASS) target -= sh.sel_excl_f;
         else k -= sh.sel_excl_u;
-        prefix = (prefix << 8) | static_cast<uint32_t>(bin < 0 ? 0 : bin);
+        prefix = (prefix << width) | static_cast<uint32_t>(bin < 0 ? 0 : bin);
         __syncthreads();
         if (shift == 0) break;
-        shift -= 8;
+        width = min(8, shift);
+        shift -= width;
     }
     if (VS) return (prefix << 16) | ((prefix & 0x8000u) ? 0u : 0xFFFFu);
     return prefix;
+}
+
+// Warp-aggregated append to a counter: one atomic per group of lanes that
+// call it together; returns this lane's slot.
+__device__ __forceinline__ int warp_append(int *counter)
+{
+    const unsigned mask = __activemask();
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(mask) - 1;
+    int base = 0;
+    if (lane == leader) base = atomicAdd(counter, __popc(mask));
+    base = __shfl_sync(mask, base, leader);
+    return base + __popc(mask & ((1u << lane) - 1u));
 }
 
 // block reduction of a float sum (result in every thread)
@@ -404,6 +451,21 @@ __device__ __forceinline__ int32_t abs_bin(float z, float s8)
     return static_cast<int32_t>(f);
 }
 
+// The smallest float z with abs_bin(z, s8) >= q (abs_bin is monotone, so the
+// set of such z is {z >= result}): a binary search over the order-preserving
+// keys of the floats from -inf to +inf.
+__device__ __forceinline__ float bin_floor_value(int32_t q, float s8)
+{
+    uint32_t lo = fkey(-INFINITY), hi = fkey(INFINITY);   // abs_bin(+inf) is the largest bin
+    if (abs_bin(-INFINITY, s8) >= q) return -INFINITY;
+    while (hi - lo > 1) {
+        const uint32_t mid = lo + (hi - lo) / 2;
+        if (abs_bin(key_value(mid), s8) >= q) hi = mid;
+        else lo = mid;
+    }
+    return key_value(hi);
+}
+
 // Pass 1 over this thread's 16-byte vectors of the staged chunk: running max
 // with the first index attaining it, and (SUM) sum exp(z - running max)
 // rescaled when the max grows.  The running max starts at a finite sentinel
@@ -411,10 +473,61 @@ __device__ __forceinline__ int32_t abs_bin(float z, float s8)
 // per-vector test; a chunk of only -inf reports -inf.
 constexpr float kSentinel = -1.0e38f;
 
+// bf16 with the sum: the two halves of each 32-bit word are one f32x2 pair,
+// so the exponent arguments and the two accumulators take packed FMA / ADD
+// (lane 0 sums the even elements, lane 1 the odd ones, in the same order as
+// the scalar form).
+template <int MODE>
+__device__ __forceinline__ float pass1_bf16_sum(const uint4 *body, int nb, int a0, float zd,
+                                                int32_t &targ, float &tsum, int32_t &tcnt)
+{
+    using E = Elt<uint16_t>;
+    float tmax = kSentinel;
+    uint64_t acc = f2_pack(0.f, 0.f);
+    const uint64_t l2 = f2_pack(kLog2e, kLog2e);
+    for (int i = threadIdx.x; i < nb; i += kThreads) {
+        const uint4 v = body[i];
+        const float vm = E::vmax(v);
+        if (vm > tmax) {
+            float x[8];
+            E::unpack(v, x);
+            int first = 7;
+#pragma unroll
+            for (int j = 7; j >= 0; --j)
+                if (x[j] == vm) first = j;
+            const float f = ex2((tmax - vm) * kLog2e);
+            acc = f2_mul(acc, f2_pack(f, f));
+            tmax = vm;
+            targ = a0 + i * 8 + first;
+        }
+        const float c0 = -tmax * kLog2e;
+        const uint64_t c2 = f2_pack(c0, c0);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float e0, e1;
+            f2_unpack(f2_fma(f2_pack(bf_lo(w[j]), bf_hi(w[j])), l2, c2), e0, e1);
+            acc = f2_add(acc, f2_pack(ex2(e0), ex2(e1)));
+        }
+        if (MODE == MODE_RELAXED) {
+            float x[8];
+            E::unpack(v, x);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) tcnt += (x[j] > zd) ? 1 : 0;
+        }
+    }
+    float s0, s1;
+    f2_unpack(acc, s0, s1);
+    tsum = s0 + s1;
+    if (tmax == kSentinel) { tmax = -INFINITY; tsum = 0.f; }
+    return tmax;
+}
+
 template <typename E, int MODE, bool SUM>
 __device__ __forceinline__ float pass1(const uint4 *body, int nb, int a0, float zd, int32_t &targ,
                                        float &tsum, int32_t &tcnt)
 {
+    if constexpr (E::BYTES == 2 && SUM) return pass1_bf16_sum<MODE>(body, nb, a0, zd, targ, tsum, tcnt);
     constexpr int VEC = E::VEC;
     float tmax = kSentinel;
     float s0 = 0.f, s1 = 0.f;     // two accumulators: independent add chains
@@ -486,6 +599,9 @@ __global__ void __launch_bounds__(256) row_info_kernel(const VerifyParams p, int
 {
     using E = Elt<TIn>;
     griddep_launch_dependents();
+    // the heavy-row queue of the sampler starts empty (the previous call's
+    // heavy kernel has completed before this kernel starts)
+    if (MODE == MODE_SAMPLE && blockIdx.x == 0 && threadIdx.x == 0) p.ws_hrows[0] = 0;
     const int lane = threadIdx.x & 31;
     if (static_cast<int>(blockIdx.x) >= row_blocks) {
         const int b = (blockIdx.x - row_blocks) * 256 + threadIdx.x;
@@ -549,22 +665,92 @@ __global__ void __launch_bounds__(256) row_info_kernel(const VerifyParams p, int
 
 // ------------------------------------------------------ stream kernel ----
 
-// exact k-th largest of the CTA's thread maxima (k <= kThreads): at least k
-// distinct elements of the chunk are >= it
+// Exact k-th largest of the CTA's thread maxima (k <= kThreads): at least k
+// distinct elements of the chunk are >= it.  A radix select over the 256
+// values whose first digit starts at the highest key bit where their minimum
+// and maximum differ.
 template <typename E>
-__device__ __forceinline__ float kth_thread_max(float thread_max, int k, float m_c, Shared &sh)
+__device__ __forceinline__ float kth_thread_max(float v, int k, float m_c, Shared &sh)
 {
+    float mn = v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
+    if ((threadIdx.x & 31) == 0) sh.red_f[threadIdx.x >> 5] = mn;
+    __syncthreads();
+    float lo = INFINITY;
+    for (int w = 0; w < kWarps; ++w) lo = fminf(lo, sh.red_f[w]);
+    __syncthreads();
     auto visit = [&](auto &&fn, float thr) {
-        if (thread_max >= thr) fn(thread_max, 0);
+        if (v >= thr) fn(v, 0);
     };
-    const uint32_t key = select_key<E, false>(visit, 0u, fkey(m_c), 0.f,
+    const uint32_t key = select_key<E, false>(visit, fkey(lo), fkey(m_c), 0.f,
                                               static_cast<uint32_t>(k), 0.f, 0.f, sh);
     return key_floor(key);
 }
 
-// One CTA per (row, chunk); plain stores of the chunk summary only.
+// CTA reduction of the per-thread (max, first argmax, sum exp(z - max),
+// count) into the chunk summary sh.part: the maximum first, then the lowest
+// index attaining it, the sums rescaled once to the maximum, the counts.
+template <int MODE>
+__device__ __forceinline__ void chunk_reduce(float tmax, int32_t targ, float tsum, int32_t tcnt,
+                                             bool need_sum, Shared &sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float wm = tmax;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
+    int32_t wa = (tmax == wm) ? targ : INT_MAX;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wa = min(wa, __shfl_xor_sync(0xFFFFFFFFu, wa, o));
+    float ws = 0.f;
+    if (need_sum) {
+        ws = (tmax > -INFINITY) ? tsum * ex2((tmax - wm) * kLog2e) : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, o);
+    }
+    int32_t wc = 0;
+    if (MODE == MODE_RELAXED) {
+        wc = tcnt;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wc += __shfl_xor_sync(0xFFFFFFFFu, wc, o);
+    }
+    if (lane == 0) {
+        sh.red_f[warp] = wm; sh.red_f[kWarps + warp] = ws;
+        sh.red_i[warp] = wa; sh.red_i[kWarps + warp] = wc;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const bool on = lane < kWarps;
+        const float m0 = on ? sh.red_f[lane] : -INFINITY;
+        float m = m0;
+#pragma unroll
+        for (int o = kWarps / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        int32_t a = (on && m0 == m) ? sh.red_i[lane] : INT_MAX;
+#pragma unroll
+        for (int o = kWarps / 2; o > 0; o >>= 1) a = min(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+        float sm_ = 0.f;
+        if (need_sum) {
+            sm_ = (on && m0 > -INFINITY) ? sh.red_f[kWarps + lane] * ex2((m0 - m) * kLog2e) : 0.f;
+#pragma unroll
+            for (int o = kWarps / 2; o > 0; o >>= 1) sm_ += __shfl_xor_sync(0xFFFFFFFFu, sm_, o);
+        }
+        int32_t cc = on ? sh.red_i[kWarps + lane] : 0;
+#pragma unroll
+        for (int o = kWarps / 2; o > 0; o >>= 1) cc += __shfl_xor_sync(0xFFFFFFFFu, cc, o);
+        if (lane == 0) {
+            sh.part.m = m; sh.part.amax = a; sh.part.s = sm_; sh.part.cnt = cc;
+            sh.part.gbest = -INFINITY; sh.part.gidx = INT_MAX; sh.part.ncand = 0;
+            sh.part.lev = -INFINITY;
+        }
+    }
+    __syncthreads();
+}
+
+// One CTA per (row, chunk); plain stores of the chunk summary only.  Many
+// short CTAs per SM keep the bulk copies in flight.
 template <typename TIn, int MODE>
-__global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const VerifyParams p)
+__global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 4 : 6)
+    stream_chunks_kernel(const VerifyParams p)
 {
     using E = Elt<TIn>;
     constexpr int VEC = E::VEC;
@@ -636,39 +822,7 @@ __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const Verify
                 need_sum);
     const float thread_max = tmax;
     const int32_t thread_arg = targ;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float om = __shfl_xor_sync(0xFFFFFFFFu, tmax, o);
-        const int32_t oa = __shfl_xor_sync(0xFFFFFFFFu, targ, o);
-        const float os = __shfl_xor_sync(0xFFFFFFFFu, tsum, o);
-        const int32_t oc = __shfl_xor_sync(0xFFFFFFFFu, tcnt, o);
-        combine(tmax, targ, tsum, tcnt, om, oa, os, oc, need_sum);
-    }
-    if (lane == 0) {
-        sh.red_f[warp] = tmax; sh.red_f[kWarps + warp] = tsum;
-        sh.red_i[warp] = targ; sh.red_i[kWarps + warp] = tcnt;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        float m = lane < kWarps ? sh.red_f[lane] : -INFINITY;
-        float sm_ = lane < kWarps ? sh.red_f[kWarps + lane] : 0.f;
-        int32_t a = lane < kWarps ? sh.red_i[lane] : INT_MAX;
-        int32_t cc = lane < kWarps ? sh.red_i[kWarps + lane] : 0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-            const int32_t oa = __shfl_xor_sync(0xFFFFFFFFu, a, o);
-            const float os = __shfl_xor_sync(0xFFFFFFFFu, sm_, o);
-            const int32_t oc = __shfl_xor_sync(0xFFFFFFFFu, cc, o);
-            combine(m, a, sm_, cc, om, oa, os, oc, need_sum);
-        }
-        if (lane == 0) {
-            sh.part.m = m; sh.part.amax = a; sh.part.s = sm_; sh.part.cnt = cc;
-            sh.part.gbest = -INFINITY; sh.part.gidx = INT_MAX; sh.part.ncand = 0;
-            sh.part.lev = -INFINITY;
-        }
-    }
-    __syncthreads();
+    chunk_reduce<MODE>(tmax, targ, tsum, tcnt, need_sum, sh);
 
     // ------------------------------------------ sampler: chunk summary --
     const int64_t rc = static_cast<int64_t>(r) * nchunk + c;
@@ -750,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const Verify
                 if (tid == 0) sh.cand_n = 0;
                 __syncthreads();
                 visit_chunk([&](float v, int32_t ix) {
-                    const int slot = atomicAdd(&sh.cand_n, 1);
+                    const int slot = warp_append(&sh.cand_n);
                     if (slot < kCandCap) { cand[slot].v = v; cand[slot].i = ix; }
                 }, lo);
                 __syncthreads();
@@ -802,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 4) stream_chunks_kernel(const Verify
     if (tid == 0) reinterpret_cast<ChunkPart *>(p.ws_part)[rc] = sh.part;
 }
 
-// ------------------------------------------------------ finish kernel ----
+// ------------------------------------------------------ row helpers ------
 
 // Visit every element of a row with value >= thr as fn(value, index): the
 // aligned body streams through two shared-memory stages by TMA bulk copies
@@ -855,23 +1009,122 @@ __device__ void visit_row(const void *row_v, int V, int h, uint8_t *stage_mem, S
     if (tid < V - t0) { const float v = E::load(row, t0 + tid); if (v >= thr) fn(v, t0 + tid); }
 }
 
+// Filter parameters of a sampler row, as every row kernel reads them.
+struct Filter {
+    float T, invT, sc;
+    bool use_k, use_m, use_p, unfiltered, pure_p;
+    __device__ __forceinline__ Filter(const RowInfo &info, int V)
+    {
+        T = info.T;
+        invT = 1.0f / T;
+        sc = invT * kLog2e;
+        use_k = info.top_k > 0 && info.top_k < V;
+        use_m = info.min_p > 0.f;
+        use_p = info.top_p < 1.f;
+        unfiltered = !use_k && !use_m && !use_p;
+        pure_p = !use_k && !use_m && use_p;
+    }
+};
+
+// The sampled token of a row from exact selects over the whole row (one
+// CTA; the fallback when candidate lists or bands overflow): survivors of
+// top-k and min-p {z >= th_S}, the nucleus of their mass {z >= th_F}, then
+// Gumbel-max over it.  Returns INT_MAX when nothing survives.
+template <typename E>
+__device__ int32_t exact_row_token(const void *row, int V, int h, float M, const RowInfo &info,
+                                   const Noise &nz, uint8_t *stage_mem, Shared &sh, uint32_t *ph)
+{
+    const Filter f(info, V);
+    const uint32_t keyM = fkey(M);
+    auto visit_all = [&](auto &&fn, float thr) {
+        visit_row<E>(row, V, h, stage_mem, sh, ph, thr, fn);
+    };
+    uint32_t key_S = f.use_m ? fkey(M + f.T * logf(info.min_p)) : 0u;
+    if (f.use_k)
+        key_S = max(key_S, select_key<E, false>(visit_all, key_S, keyM, 0.f,
+                                                static_cast<uint32_t>(info.top_k), M, f.sc, sh));
+    uint32_t key_F = key_S;
+    if (f.use_p) {
+        float w = 0.f;
+        const uint32_t kS = key_S;
+        visit_all([&](float v, int32_t) {
+            if (fkey(v) >= kS) w += ex2((v - M) * f.sc);
+        }, key_floor(key_S));
+        const float Wt = block_sum(w, sh);
+        key_F = max(key_S, select_key<E, true>(visit_all, key_S, keyM, info.top_p * Wt, 0u, M,
+                                               f.sc, sh));
+    }
+    GumbelScorer gs{f.invT, nz, 0xFFFFFFFFu, make_uint4(0, 0, 0, 0)};
+    float best = -INFINITY;
+    int32_t bi = INT_MAX;
+    const uint32_t kF = key_F;
+    visit_all([&](float v, int32_t ix) {
+        if (fkey(v) >= kF) keep_best(gs(v, ix), ix, best, bi);
+    }, key_floor(key_F));
+    block_best(best, bi, sh);
+    return bi;
+}
+
+// The request chain, run by warp 0 of the CTA that settles row r's token:
+// the CTA finishing the last row of the request (atomic ticket) runs the
+// accept-while-equal prefix scan with one ballot and writes the request's
+// tokens and the optional prefix-acceptance counters.
+template <int MODE>
+__device__ __forceinline__ void request_chain(const VerifyParams &p, const RowInfo &info, int r)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t t = 0;
+    if (lane == 0) {
+        fence_acq_rel_gpu();
+        t = atomicAdd(p.ws_ticket + info.b, 1u);
+        if (t == static_cast<uint32_t>(info.k_b)) fence_acq_rel_gpu();
+    }
+    t = __shfl_sync(0xFFFFFFFFu, t, 0);
+    if (t != static_cast<uint32_t>(info.k_b)) return;
+    const int b = info.b, k = info.k_b, r0 = r - info.pos;
+    const int j = lane;
+    const int32_t yj = (j <= k) ? __ldcg(p.ws_tok + r0 + j) : -1;
+    const int32_t dj = (j < k) ? __ldg(p.draft_ids + r0 + j) : -1;
+    bool ok;
+    if (MODE == MODE_RELAXED) ok = (j < k) && __ldcg(p.ws_flag + r0 + j) != 0;
+    else ok = (j < k) && (yj == dj);
+    const unsigned mism = __ballot_sync(0xFFFFFFFFu, (j < k) && !ok);
+    const int a = mism ? (__ffs(mism) - 1) : k;
+    const int32_t tok = __shfl_sync(0xFFFFFFFFu, yj, a);
+    if (j <= p.k_max)
+        p.out_tokens[static_cast<int64_t>(b) * (p.k_max + 1) + j] = (j < a) ? dj : (j == a ? tok : -1);
+    if (j == 0) {
+        p.accepted_len[b] = a;
+        p.next_token[b] = tok;
+        p.ws_ticket[b] = 0u;
+        set_status(p.status, static_cast<uint32_t>(info.bad));
+        if (p.hist) atomicAdd(reinterpret_cast<unsigned long long *>(p.hist + a), 1ull);
+    }
+    if (j < p.k_max) {
+        if (p.acc && a > j) atomicAdd(reinterpret_cast<unsigned long long *>(p.acc + j), 1ull);
+        if (p.ver && k > j) atomicAdd(reinterpret_cast<unsigned long long *>(p.ver + j), 1ull);
+    }
+}
+
+// ------------------------------------------------------ finish kernel ----
+
 // One CTA per packed row, after the stream kernel: combine the chunk
-// summaries, pick the row's token, write the row results, run the chain.
+// summaries, pick the row's token, write the row results, run the chain;
+// rows that need their logits again are queued for the heavy kernel.
 template <typename TIn, int MODE>
-__global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParams p)
+__global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyParams p)
 {
     using E = Elt<TIn>;
     extern __shared__ __align__(128) uint8_t smem[];
     Shared &sh = *reinterpret_cast<Shared *>(smem);
     ChunkPart *parts = reinterpret_cast<ChunkPart *>(smem + sizeof(Shared));       // [kMaxChunks]
     Cand *band = reinterpret_cast<Cand *>(parts + kMaxChunks);                     // [kBandCap]
-    uint8_t *stage_mem = reinterpret_cast<uint8_t *>(band + kBandCap);             // 2 x kRowStage
-    Cand *lst = reinterpret_cast<Cand *>(stage_mem);                               // or [kListCap]
-    __shared__ uint32_t ph[2];
+    Cand *lst = band + kBandCap;                                                   // [kListCap]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = blockIdx.x;
     const int nchunk = p.nchunk;
 
+    griddep_launch_dependents();
     griddep_wait();                        // the stream kernel's stores are visible
     if (tid == 0) {
         if (MODE != MODE_CONF) {
@@ -883,11 +1136,7 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
             inf.sel = p.selected ? static_cast<uint32_t>(__ldg(p.selected + r)) : 0xFFFFFFFFu;
             sh.info = inf;
         }
-        sh.timeout = 0;
-        mbar_init(&sh.mbar[0], 1);
-        mbar_init(&sh.mbar[1], 1);
-        fence_mbar_init();
-        ph[0] = ph[1] = 0u;
+        sh.heavy = 0;
     }
     if (tid < nchunk) {
         const ChunkPart *rp = reinterpret_cast<const ChunkPart *>(p.ws_part) + static_cast<int64_t>(r) * nchunk;
@@ -902,8 +1151,6 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
     const RowInfo &info = sh.info;
     if (!info.valid) return;
     const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
-    const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row) & 15u);
-    const int h = min(mis ? static_cast<int>((16u - mis) / E::BYTES) : 0, p.V);
     const bool need_sum = (MODE == MODE_CONF) || (p.row_lse != nullptr);
 
     // combine the chunk summaries (warp 0; chunk order fixed)
@@ -933,26 +1180,19 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
     if (MODE == MODE_RELAXED)
         flag = (info.draft >= 0 && info.draft < p.V && sh.CNT < info.K) ? 1 : 0;
 
+    HeavyRec hrec = {};                    // thread 0: the queued row's record
     if (MODE == MODE_SAMPLE && info.T > 0.f && M > -INFINITY) {
-        const float T = info.T;
-        const float invT = 1.0f / T;
-        const float sc = invT * kLog2e;
-        const bool use_k = info.top_k > 0 && info.top_k < p.V;
-        const bool use_m = info.min_p > 0.f;
-        const bool use_p = info.top_p < 1.f;
-        const bool unfiltered = !use_k && !use_m && !use_p;
-        const bool pure_p = !use_k && !use_m && use_p;
+        const Filter f(info, p.V);
+        const float T = f.T, sc = f.sc;
         const uint32_t keyM = fkey(M);
-        GumbelScorer gs{invT, Noise{static_cast<uint32_t>(info.pos), info.rid, p.step, info.seed_lo,
-                                    info.seed_hi},
+        GumbelScorer gs{f.invT, Noise{static_cast<uint32_t>(info.pos), info.rid, p.step,
+                                      info.seed_lo, info.seed_hi},
                         0xFFFFFFFFu, make_uint4(0, 0, 0, 0)};
         float best = -INFINITY;
         int32_t bi = INT_MAX;
         auto score_all = [&](float v, int32_t ix) { keep_best(gs(v, ix), ix, best, bi); };
-        auto visit_all = [&](auto &&fn, float thr) {
-            visit_row<E>(row, p.V, h, stage_mem, sh, ph, thr, fn);
-        };
-        if (unfiltered) {
+        int heavy = 0;
+        if (f.unfiltered) {
             for (int q = tid; q < nchunk; q += kThreads) keep_best(parts[q].gbest, parts[q].gidx, best, bi);
             block_best(best, bi, sh);
         } else {
@@ -1010,7 +1250,7 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
                     }
                 }
             };
-            if (pure_p) {
+            if (f.pure_p) {
                 // ---- top-p alone: bracket the boundary with the bins ----
                 const float s8 = bin_scale(T);
                 if (tid == 0) {
@@ -1029,9 +1269,9 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
                 __syncthreads();
                 const float target = info.top_p * sh.W;
                 const int32_t J = sh.J;
-                bool whole = sh.nobins != 0;
+                heavy = sh.nobins ? kHeavyWhole : 0;
                 int32_t qin = 0, qband = 0;
-                if (!whole) {
+                if (!heavy) {
                     // combined mass of absolute bin J - t, then C(t) = mass of
                     // bins J - t .. J (thread t)
                     float hb = 0.f;
@@ -1056,44 +1296,36 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
                     for (int w = 0; w < warp; ++w) cum += wt[w];
                     // bins 0..a are surely inside (mass above < target), bins
                     // from b on surely outside; the band between is settled
-                    // exactly below
+                    // exactly
                     const int n_in = __syncthreads_count(tid < kBins && cum < target * (1.f - kMassTol));
                     const int n_out = __syncthreads_count(tid < kBins && cum >= target * (1.f + kMassTol));
                     const int a = n_in - 1, b = kBins - n_out;
-                    if (b >= kBins) whole = true;       // the nucleus reaches below the bins
+                    if (b >= kBins) heavy = kHeavyWhole;      // the nucleus reaches below the bins
                     qin = J - a;
                     qband = J - b;
                 }
-                if (!whole) {
-                    // the lists cover the band when every value below the
-                    // highest list level falls in a bin below the band
-                    const bool from_lists = staged && abs_bin(sh.theta, s8) < qband;
-                    if (from_lists) stage_lists();
+                // the lists cover the band when every value below the highest
+                // list level falls in a bin below the band
+                if (!heavy && !(staged && abs_bin(sh.theta, s8) < qband)) heavy = kHeavyBand;
+                if (!heavy) {
+                    stage_lists();
                     if (tid == 0) sh.cand_n = 0;
                     __syncthreads();
                     float mass_in = 0.f;
-                    auto classify = [&](float v, int32_t ix) {
+                    visit_lst([&](float v, int32_t ix) {
                         const int32_t qz = abs_bin(v, s8);
                         if (qz >= qin) {
                             mass_in += ex2((v - M) * sc);
                             score_all(v, ix);
                         } else if (qz >= qband) {
-                            const int slot = atomicAdd(&sh.cand_n, 1);
+                            const int slot = warp_append(&sh.cand_n);
                             if (slot < kBandCap) { band[slot].v = v; band[slot].i = ix; }
                         }
-                    };
-                    // values below thr lie in bins below the band
-                    const float thr = (J > (1 << 21) || J < -(1 << 21))
-                                          ? -INFINITY
-                                          : static_cast<float>(qband - 1) / s8;
-                    if (from_lists) visit_lst(classify, thr);
-                    else visit_all(classify, thr);
+                    }, -INFINITY);
                     mass_in = block_sum(mass_in, sh);
-                    const int nband = sh.cand_n;
+                    const int nband = min(sh.cand_n, kBandCap);
                     const float tgt = target - mass_in;
-                    if (nband > kBandCap) {
-                        whole = true;
-                    } else if (nband > 0 && tgt > 0.f) {
+                    if (nband > 0 && tgt > 0.f) {
                         uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
                         for (int i = tid; i < nband; i += kThreads) {
                             const uint32_t k = fkey(band[i].v);
@@ -1110,36 +1342,40 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
                             if (fkey(v) >= kF) score_all(v, ix);
                         }, -INFINITY);
                     }
+                    block_best(best, bi, sh);
+                } else if (tid == 0) {
+                    hrec.mode = heavy;
+                    hrec.amax = AMAX;
+                    hrec.qin = qin;
+                    hrec.qband = qband;
+                    hrec.M = M;
+                    hrec.target = target;
+                    if (heavy == kHeavyBand) {
+                        hrec.zin = bin_floor_value(qin, s8);
+                        hrec.zband = bin_floor_value(qband, s8);
+                    }
                 }
-                if (whole) {
-                    // exact mass select over the whole row
-                    best = -INFINITY;
-                    bi = INT_MAX;
-                    const uint32_t kF = select_key<E, true>(visit_all, 0u, keyM, target, 0u, M, sc, sh);
-                    visit_all([&](float v, int32_t ix) {
-                        if (fkey(v) >= kF) score_all(v, ix);
-                    }, key_floor(kF));
-                }
-                block_best(best, bi, sh);
+            } else if (sh.overflow) {
+                // ---- top-k / min-p with an overflowed list ----
+                heavy = kHeavyWhole;
+                if (tid == 0) { hrec.mode = heavy; hrec.amax = AMAX; hrec.M = M; }
             } else {
                 // ---- top-k and / or min-p (then top-p over the survivors) --
-                const bool whole = sh.overflow != 0;
                 if (staged) stage_lists();
                 auto visit = [&](auto &&fn, float thr) {
-                    if (whole) visit_all(fn, thr);
-                    else if (staged) visit_lst(fn, thr);
+                    if (staged) visit_lst(fn, thr);
                     else visit_gl(fn, thr);
                 };
-                const float th_m = use_m ? M + T * logf(info.min_p) : -INFINITY;
-                uint32_t key_S = use_m ? fkey(th_m) : 0u;
+                const float th_m = f.use_m ? M + T * logf(info.min_p) : -INFINITY;
+                uint32_t key_S = f.use_m ? fkey(th_m) : 0u;
                 // every list element lies above its chunk's level
-                const uint32_t lo_k = whole ? key_S : max(key_S, sh.lkey);
-                if (use_k && (whole || n_list >= info.top_k))
+                const uint32_t lo_k = max(key_S, sh.lkey);
+                if (f.use_k && n_list >= info.top_k)
                     key_S = max(key_S, select_key<E, false>(visit, lo_k, keyM, 0.f,
                                                             static_cast<uint32_t>(info.top_k), M,
                                                             sc, sh));
                 uint32_t key_F = key_S;
-                if (use_p) {
+                if (f.use_p) {
                     float w = 0.f;
                     const uint32_t kS = key_S;
                     visit([&](float v, int32_t) {
@@ -1156,10 +1392,19 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
                 block_best(best, bi, sh);
             }
         }
+        if (heavy && tid == 0) {
+            // queue the row: record in the row's bin area, then the list slot
+            reinterpret_cast<HeavyRec *>(p.ws_bins + static_cast<int64_t>(r) * nchunk * kBins)[0] = hrec;
+            const int slot = atomicAdd(p.ws_hrows, 1);
+            p.ws_hrows[1 + slot] = r;
+            sh.heavy = 1;
+        }
         y = (bi == INT_MAX) ? AMAX : bi;
     }
 
     // ---------------------------------------------------- row results ---
+    __syncthreads();
+    const bool queued = sh.heavy != 0;
     if (tid == 0) {
         const float S = sh.S;
         if (p.row_max) p.row_max[r] = M;
@@ -1176,48 +1421,281 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
             }
             p.conf[r] = cf;
             p.draft_token[r] = s;
-        } else {
+        } else if (!queued) {
             if (p.row_token) p.row_token[r] = y;
             p.ws_tok[r] = y;
             if (MODE == MODE_RELAXED) p.ws_flag[r] = flag;
         }
-        if (sh.timeout) set_status(p.status, SPEC_STATUS_TIMEOUT);
     }
+    if (MODE != MODE_CONF && !queued && warp == 0) request_chain<MODE>(p, info, r);
+}
 
-    // ------------------------------- request chain (last row of request) --
-    if (MODE != MODE_CONF && warp == 0) {
-        uint32_t t = 0;
-        if (lane == 0) {
-            fence_acq_rel_gpu();
-            t = atomicAdd(p.ws_ticket + info.b, 1u);
-            if (t == static_cast<uint32_t>(info.k_b)) fence_acq_rel_gpu();
+// ------------------------------------------------------- heavy kernel ----
+
+// Persistent over the chunks of the rows the finish kernel queued.  A row
+// queued for its band: every chunk is staged by TMA; its values at or above
+// the band's upper edge are in the nucleus, the values in the band are
+// collected; both are compacted in shared memory (counts, a CTA scan, a
+// scatter: no per-element branches that diverge) and the nucleus is scored
+// with all lanes busy; each chunk's band values go to its own list.  The CTA
+// finishing the row's last chunk (atomic ticket) settles the band with an
+// exact mass select and runs the request chain.  A row queued whole: the CTA
+// of its first chunk runs the exact selects over the row.
+template <typename TIn>
+__global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyParams p)
+{
+    using E = Elt<TIn>;
+    constexpr int VEC = E::VEC;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *chunk = smem;                                   // one chunk, or two row stages
+    Shared &sh = *reinterpret_cast<Shared *>(smem + kChunkBytes);
+    Cand *sure = reinterpret_cast<Cand *>(reinterpret_cast<uint8_t *>(&sh) + sizeof(Shared));
+    Cand *band = sure + kSureCap;
+    __shared__ uint32_t ph[2];
+    __shared__ HeavyRec rec_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nchunk = p.nchunk;
+
+    griddep_wait();                         // the finish kernel's queue is complete
+    const int n_heavy = __ldcg(p.ws_hrows);
+    const int64_t n_items = static_cast<int64_t>(n_heavy) * nchunk;
+    if (static_cast<int64_t>(blockIdx.x) >= n_items) return;
+    if (tid == 0) {
+        mbar_init(&sh.mbar[0], 1);
+        mbar_init(&sh.mbar[1], 1);
+        fence_mbar_init();
+        ph[0] = ph[1] = 0u;
+        sh.timeout = 0;
+    }
+    for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int hr = static_cast<int>(it / nchunk);
+        const int c = static_cast<int>(it - static_cast<int64_t>(hr) * nchunk);
+        const int r = __ldcg(p.ws_hrows + 1 + hr);
+        float *area = p.ws_bins + static_cast<int64_t>(r) * nchunk * kBins;
+        const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
+        const ChunkGeom g = chunk_geom<E>(row, c, p.V);
+        if (tid == 0) {
+            // the chunk's copy first (in bounds for any queued row), then the
+            // row's record and parameters while it is in flight
+            const uint32_t bytes = static_cast<uint32_t>(g.nb) * 16u;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&sh.mbar[0], bytes);
+            if (bytes) bulk_g2s(chunk, row + g.a0, bytes, &sh.mbar[0]);
+            sh.info = reinterpret_cast<const RowInfo *>(p.ws_info)[r];
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(area));
+            const float4 b = __ldcg(reinterpret_cast<const float4 *>(area) + 1);
+            rec_s.mode = __float_as_int(a.x);
+            rec_s.qin = __float_as_int(a.y);
+            rec_s.qband = __float_as_int(a.z);
+            rec_s.amax = __float_as_int(a.w);
+            rec_s.M = b.x;
+            rec_s.target = b.y;
+            rec_s.zin = b.z;
+            rec_s.zband = b.w;
+            sh.last = 0;
         }
-        t = __shfl_sync(0xFFFFFFFFu, t, 0);
-        if (t == static_cast<uint32_t>(info.k_b)) {
-            const int b = info.b, k = info.k_b, r0 = r - info.pos;
-            const int j = lane;
-            const int32_t yj = (j <= k) ? __ldcg(p.ws_tok + r0 + j) : -1;
-            const int32_t dj = (j < k) ? __ldg(p.draft_ids + r0 + j) : -1;
-            bool ok;
-            if (MODE == MODE_RELAXED) ok = (j < k) && __ldcg(p.ws_flag + r0 + j) != 0;
-            else ok = (j < k) && (yj == dj);
-            const unsigned mism = __ballot_sync(0xFFFFFFFFu, (j < k) && !ok);
-            const int a = mism ? (__ffs(mism) - 1) : k;
-            const int32_t tok = __shfl_sync(0xFFFFFFFFu, yj, a);
-            if (j <= p.k_max)
-                p.out_tokens[static_cast<int64_t>(b) * (p.k_max + 1) + j] = (j < a) ? dj : (j == a ? tok : -1);
-            if (j == 0) {
-                p.accepted_len[b] = a;
-                p.next_token[b] = tok;
-                p.ws_ticket[b] = 0u;
-                set_status(p.status, static_cast<uint32_t>(info.bad));
-                if (p.hist) atomicAdd(reinterpret_cast<unsigned long long *>(p.hist + a), 1ull);
+        float xe = -INFINITY;
+        int32_t ie = INT_MAX;
+        if (tid < g.n_extra) {
+            ie = (tid < g.n_head) ? g.e0 + tid : g.a1 + (tid - g.n_head);
+            xe = E::load(row, ie);
+        }
+        if (tid == 0) {
+            if (!mbar_wait(&sh.mbar[0], ph[0])) {
+                sh.timeout = 1;
+                set_status(p.status, SPEC_STATUS_TIMEOUT);
             }
-            if (j < p.k_max) {
-                if (p.acc && a > j) atomicAdd(reinterpret_cast<unsigned long long *>(p.acc + j), 1ull);
-                if (p.ver && k > j) atomicAdd(reinterpret_cast<unsigned long long *>(p.ver + j), 1ull);
+            ph[0] ^= 1u;
+        }
+        __syncthreads();
+        const RowInfo info = sh.info;
+        const HeavyRec rec = rec_s;
+        const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row) & 15u);
+        const int h = min(mis ? static_cast<int>((16u - mis) / E::BYTES) : 0, p.V);
+        const Noise nz{static_cast<uint32_t>(info.pos), info.rid, p.step, info.seed_lo, info.seed_hi};
+        const Filter f(info, p.V);
+        const float M = rec.M;
+        int32_t y = INT_MAX;
+        bool settle = false;
+        if (rec.mode == kHeavyWhole) {
+            if (c == 0) {
+                y = exact_row_token<E>(row, p.V, h, M, info, nz, chunk, sh, ph);
+                settle = true;
+            }
+        } else {
+            // ---- one chunk of a band row ----
+            const float sc = f.sc;
+            const float zin = rec.zin, zband = rec.zband;
+            float2 *blist = reinterpret_cast<float2 *>(p.ws_cand) +
+                            static_cast<int64_t>(r) * nchunk * kCandCap;
+            float mass = 0.f, best = -INFINITY;
+            int32_t bi = INT_MAX;
+            const uint4 *body = reinterpret_cast<const uint4 *>(chunk);
+            // count this thread's nucleus (z >= zin) and band (zband <= z <
+            // zin) values: compares only
+            int ns = 0, nbd = 0;
+            for (int i = tid; i < g.nb; i += kThreads) {
+                const uint4 v = body[i];
+                if (!(E::vmax(v) >= zband)) continue;
+                float x[VEC];
+                E::unpack(v, x);
+#pragma unroll
+                for (int q = 0; q < VEC; ++q) {
+                    ns += (x[q] >= zin) ? 1 : 0;
+                    nbd += (x[q] >= zband && !(x[q] >= zin)) ? 1 : 0;
+                }
+            }
+            if (tid < g.n_extra) {
+                ns += (xe >= zin) ? 1 : 0;
+                nbd += (xe >= zband && !(xe >= zin)) ? 1 : 0;
+            }
+            // exclusive offsets of both counts across the CTA
+            int os = ns, ob = nbd;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int a1 = __shfl_up_sync(0xFFFFFFFFu, os, o);
+                const int b1 = __shfl_up_sync(0xFFFFFFFFu, ob, o);
+                if (lane >= o) { os += a1; ob += b1; }
+            }
+            if (lane == 31) { sh.red_i[warp] = os; sh.red_i[kWarps + warp] = ob; }
+            __syncthreads();
+            int ws = 0, wb = 0, ts = 0, tb = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                if (w < warp) { ws += sh.red_i[w]; wb += sh.red_i[kWarps + w]; }
+                ts += sh.red_i[w];
+                tb += sh.red_i[kWarps + w];
+            }
+            os += ws - ns;
+            ob += wb - nbd;
+            // scatter: nucleus values to `sure` (scored directly past its
+            // capacity), band values to `band`
+            auto place = [&](float v, int32_t ix) {
+                if (v >= zin) {
+                    if (os < kSureCap) { sure[os].v = v; sure[os].i = ix; }
+                    else { mass += ex2((v - M) * sc); keep_best(nz.score(v, ix, f.invT), ix, best, bi); }
+                    ++os;
+                } else if (v >= zband) {
+                    if (ob < kCandCap) { band[ob].v = v; band[ob].i = ix; }
+                    ++ob;
+                }
+            };
+            if (ns + nbd > 0) {
+                for (int i = tid; i < g.nb; i += kThreads) {
+                    const uint4 v = body[i];
+                    if (!(E::vmax(v) >= zband)) continue;
+                    float x[VEC];
+                    E::unpack(v, x);
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) place(x[q], g.a0 + i * VEC + q);
+                }
+                if (tid < g.n_extra) place(xe, ie);
+            }
+            __syncthreads();
+            // the chunk's band values to its own list (no global atomics)
+            float2 *clist = blist + static_cast<int64_t>(c) * kCandCap;
+            for (int i = tid; i < min(tb, kCandCap); i += kThreads)
+                clist[i] = make_float2(band[i].v, __int_as_float(band[i].i));
+            // the compacted nucleus values: mass and scores with all lanes busy
+            const int n_sure = min(ts, kSureCap);
+            for (int i = tid; i < n_sure; i += kThreads) {
+                const Cand e = sure[i];
+                mass += ex2((e.v - M) * sc);
+                keep_best(nz.score(e.v, e.i, f.invT), e.i, best, bi);
+            }
+            block_best(best, bi, sh);
+            mass = block_sum(mass, sh);
+            if (tid == 0) {
+                HeavyPart hp;
+                hp.best = best;
+                hp.bi = bi;
+                hp.mass = mass;
+                hp.nband = tb;
+                reinterpret_cast<HeavyPart *>(area + 8)[c] = hp;
+                // publish the chunk's results and list, then count
+                fence_acq_rel_gpu();
+                const uint32_t t = atomicAdd(p.ws_rticket + r, 1u);
+                if (t == static_cast<uint32_t>(nchunk - 1)) {
+                    fence_acq_rel_gpu();
+                    sh.last = 1;
+                }
+            }
+            __syncthreads();
+            if (sh.last) {
+                // ---- the row's last chunk: settle the band ----
+                if (tid == 0) {
+                    const HeavyPart *hp = reinterpret_cast<const HeavyPart *>(area + 8);
+                    float bsum = 0.f, bb = -INFINITY;
+                    int32_t bbi = INT_MAX, tot = 0, ovf = 0;
+                    for (int q = 0; q < nchunk; ++q) {
+                        const float4 e = __ldcg(reinterpret_cast<const float4 *>(hp + q));
+                        bsum += e.z;
+                        keep_best(e.x, __float_as_int(e.y), bb, bbi);
+                        const int nq = __float_as_int(e.w);
+                        sh.offs[q] = tot;
+                        ovf |= (nq > kCandCap);
+                        tot += min(nq, kCandCap);
+                    }
+                    sh.offs[nchunk] = tot;
+                    sh.W = bsum;
+                    sh.red_f[0] = bb;
+                    sh.red_i[0] = bbi;
+                    sh.total = tot;
+                    sh.overflow = ovf;
+                    p.ws_rticket[r] = 0u;
+                }
+                __syncthreads();
+                const float mass_in = sh.W;
+                best = sh.red_f[0];
+                bi = sh.red_i[0];
+                const int nband = sh.total;
+                const bool ovf = sh.overflow != 0;
+                __syncthreads();
+                if (ovf || nband > kBandCap) {
+                    y = exact_row_token<E>(row, p.V, h, M, info, nz, chunk, sh, ph);
+                } else {
+                    const float tgt = rec.target - mass_in;
+                    if (nband > 0 && tgt > 0.f) {
+                        for (int e = tid; e < nband; e += kThreads) {
+                            int q = 0;
+                            while (sh.offs[q + 1] <= e) ++q;
+                            const float2 v = __ldcg(blist + static_cast<int64_t>(q) * kCandCap + (e - sh.offs[q]));
+                            band[e].v = v.x;
+                            band[e].i = __float_as_int(v.y);
+                        }
+                        __syncthreads();
+                        uint32_t kmn = 0xFFFFFFFFu, kmx = 0u;
+                        for (int i = tid; i < nband; i += kThreads) {
+                            const uint32_t k = fkey(band[i].v);
+                            kmn = min(kmn, k);
+                            kmx = max(kmx, k);
+                        }
+                        block_minmax(kmn, kmx, sh);
+                        auto visit_band = [&](auto &&fn, float t2) {
+                            for (int i = tid; i < nband; i += kThreads)
+                                if (band[i].v >= t2) fn(band[i].v, band[i].i);
+                        };
+                        const uint32_t kF = select_key<E, true>(visit_band, kmn, kmx, tgt, 0u, M, sc, sh);
+                        visit_band([&](float v, int32_t ix) {
+                            if (fkey(v) >= kF) keep_best(nz.score(v, ix, f.invT), ix, best, bi);
+                        }, -INFINITY);
+                    }
+                    block_best(best, bi, sh);
+                    y = bi;
+                }
+                settle = true;
             }
         }
+        if (settle) {
+            if (y == INT_MAX) y = rec.amax;
+            if (tid == 0) {
+                if (p.row_token) p.row_token[r] = y;
+                p.ws_tok[r] = y;
+                if (sh.timeout) set_status(p.status, SPEC_STATUS_TIMEOUT);
+            }
+            __syncthreads();
+            if (warp == 0) request_chain<MODE_SAMPLE>(p, info, r);
+        }
+        __syncthreads();
     }
 }
 
@@ -1238,23 +1716,47 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     if (MODE == MODE_SAMPLE)
         smem += static_cast<size_t>(kCandCap) * sizeof(Cand) + static_cast<size_t>(kWarps) * kBins * 4;
     const size_t smem_fin = sizeof(Shared) + kMaxChunks * sizeof(ChunkPart) +
-                            static_cast<size_t>(kBandCap) * sizeof(Cand) + 2 * kRowStage;
+                            static_cast<size_t>(kBandCap + kListCap) * sizeof(Cand);
+    const size_t smem_heavy = kChunkBytes + sizeof(Shared) +
+                              static_cast<size_t>(kSureCap + kBandCap) * sizeof(Cand);
     auto kstream = stream_chunks_kernel<TIn, MODE>;
     auto kfin = finish_rows_kernel<TIn, MODE>;
-    // raise the dynamic shared-memory limits once per device
+    auto kheavy = heavy_rows_kernel<TIn>;
+    // raise the dynamic shared-memory limits, prefer shared memory over L1
+    // (the row kernels want as many resident CTAs as it allows) and read the
+    // SM count, once per device
     static bool done[64] = {false};
+    static int sms[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !done[dev]) {
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!done[dev]) {
         e = cudaFuncSetAttribute(kstream, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kstream, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kfin, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem_fin));
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) done[dev] = true;
+        e = cudaFuncSetAttribute(kfin, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+        if (MODE == MODE_SAMPLE) {
+            e = cudaFuncSetAttribute(kheavy, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem_heavy));
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(kheavy, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+            if (e != cudaSuccess) return e;
+        }
+        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
     }
+    const int nsm = sms[dev] > 0 ? sms[dev] : 1;
     const int rows = (MODE == MODE_CONF) ? p.n_rows : p.R_cap;
     if (MODE != MODE_CONF) {
         const int row_blocks = static_cast<int>((static_cast<int64_t>(p.R_cap) * 32 + 255) / 256);
@@ -1266,8 +1768,9 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // one CTA per (row, chunk); the entry points bound rows * nchunk by 2^31 - 1
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(rows) * static_cast<unsigned>(p.nchunk), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(rows) * p.nchunk), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -1282,7 +1785,17 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     cf.stream = stream;
     cf.attrs = attr;
     cf.numAttrs = 1;
-    return cudaLaunchKernelEx(&cf, kfin, p);
+    e = cudaLaunchKernelEx(&cf, kfin, p);
+    if (e != cudaSuccess || MODE != MODE_SAMPLE) return e;
+    // heavy rows: persistent over whatever the finish kernel queued
+    cudaLaunchConfig_t ch = {};
+    ch.gridDim = dim3(static_cast<unsigned>(3 * nsm), 1, 1);
+    ch.blockDim = dim3(kThreads, 1, 1);
+    ch.dynamicSmemBytes = smem_heavy;
+    ch.stream = stream;
+    ch.attrs = attr;
+    ch.numAttrs = 1;
+    return cudaLaunchKernelEx(&ch, kheavy, p);
 }
 
 cudaError_t launch_verify(int mode, int dtype, const VerifyParams &p, cudaStream_t stream)
