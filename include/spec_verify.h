@@ -155,6 +155,32 @@ SPEC_API int spec_verify_greedy(const spec_batch *batch, const spec_outputs *out
                        void *workspace, size_t workspace_bytes, spec_stream stream);
 
 /*
+ * spec_verify_greedy for callers that cannot allocate device memory.  This
+ * entry point has no counterpart in the method; it is a convenience of this
+ * library.  Some callers cannot call cudaMalloc at the point where they
+ * verify: a plugin running inside an engine that owns the whole device
+ * memory pool, or a serving loop that forbids allocation (and its latency or
+ * failure) once it is running.  They pass inputs and outputs only; the
+ * workspace is a scratch array of SPEC_NOALLOC_SCRATCH_BYTES compiled into
+ * the library, which every GPU that loads the library holds until the
+ * process exits.
+ *
+ * Same inputs, outputs and results as spec_verify_greedy.  A batch whose
+ * workspace (spec_workspace_bytes(R_cap, B, V, dtype, 0)) exceeds
+ * SPEC_NOALLOC_SCRATCH_BYTES returns SPEC_ERR_WORKSPACE before any launch
+ * (about 250 KiB suffice for 640 rows of a 152064-token vocabulary).
+ * The first call on each device looks up the array's device address (with
+ * that device current), so make that first call before any stream capture.
+ * Every call shares the one array: calls that can overlap on the GPU (two
+ * streams, two host threads) race and must be ordered by the caller.  Each
+ * call clears the array's ticket words itself on its stream before its
+ * kernels run.  Nothing is allocated or freed.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+SPEC_API int spec_verify_greedy_noalloc(const spec_batch *batch, const spec_outputs *out,
+                                        spec_stream stream);
+
+/*
  * A5: relaxed top-K acceptance with a strict prefix (vSpec README
  * §"支持范围", §"EAGLE 功能").  Draft d of row r is accepted iff d is in
  * [0, V) and #{i : z_r[i] > z_r[d]} < relaxed_k[b] (ties with the K-th value

@@ -31,7 +31,8 @@ STATUS_BAD_RELAXED_K = 0x40
 STATUS_BAD_BUDGET = 0x80
 STATUS_TIMEOUT = 0x100
 
-EXPORTS = ["spec_workspace_bytes", "spec_draft_workspace_bytes", "spec_verify_greedy", "spec_verify_relaxed_topk",
+EXPORTS = ["spec_workspace_bytes", "spec_draft_workspace_bytes", "spec_verify_greedy",
+           "spec_verify_greedy_noalloc", "spec_verify_relaxed_topk",
            "spec_verify_sample", "spec_draft_confidence", "spec_prefix_stats",
            "spec_result_string", "spec_last_cuda_error", "spec_abi_version"]
 
@@ -90,6 +91,7 @@ def load_library(path: Optional[str] = None) -> C.CDLL:
     L.spec_draft_workspace_bytes.restype = C.c_size_t
     L.spec_workspace_bytes.restype = C.c_size_t
     L.spec_verify_greedy.argtypes = [C.POINTER(Batch), C.POINTER(Outputs), vp, C.c_size_t, vp]
+    L.spec_verify_greedy_noalloc.argtypes = [C.POINTER(Batch), C.POINTER(Outputs), vp]
     L.spec_verify_relaxed_topk.argtypes = [C.POINTER(Batch), vp, C.POINTER(Outputs), vp,
                                            C.c_size_t, vp]
     L.spec_verify_sample.argtypes = [C.POINTER(Batch), C.POINTER(Sampling), C.POINTER(Outputs),
@@ -97,7 +99,8 @@ def load_library(path: Optional[str] = None) -> C.CDLL:
     L.spec_draft_confidence.argtypes = [C.POINTER(Draft), C.POINTER(Allocation), vp, C.c_size_t,
                                         vp]
     L.spec_prefix_stats.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp]
-    for f in ["spec_verify_greedy", "spec_verify_relaxed_topk", "spec_verify_sample",
+    for f in ["spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_relaxed_topk",
+              "spec_verify_sample",
               "spec_draft_confidence", "spec_prefix_stats", "spec_abi_version"]:
         getattr(L, f).restype = C.c_int
     L.spec_result_string.argtypes = [C.c_int]
@@ -219,6 +222,20 @@ def verify_greedy(logits, cu_rows, draft_ids, *, V: int, B: int, k_max: int,
     b = _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids)
     o, res = _outputs(B, k_max, R_cap, logits.device, rows, stats)
     _check(L.spec_verify_greedy(C.byref(b), C.byref(o), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return res
+
+
+def verify_greedy_noalloc(logits, cu_rows, draft_ids, *, V: int, B: int, k_max: int,
+                          R_cap: Optional[int] = None, rows: bool = True, stats=None,
+                          stream=None) -> dict:
+    """spec_verify_greedy_noalloc: greedy verification for callers that cannot
+    allocate device memory; the library's built-in scratch array stands in
+    for the workspace.  Calls that overlap on the GPU race on that array."""
+    L = load_library()
+    R_cap = R_cap or B * (k_max + 1)
+    b = _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids)
+    o, res = _outputs(B, k_max, R_cap, logits.device, rows, stats)
+    _check(L.spec_verify_greedy_noalloc(C.byref(b), C.byref(o), _stream(stream)))
     return res
 
 

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -140,6 +141,31 @@ int run_verify(int mode, const spec_batch *b, VerifyParams &p, cudaStream_t s)
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 
+// Built-in scratch of spec_verify_greedy_noalloc: a device array of the
+// library (zero at load), its device address looked up once per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64] = {};
+
+// Device address of the scratch array on the current device (the host-side
+// name of the array is not a device address; only this lookup gives one).
+int noalloc_scratch(void **ptr)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= 64) return SPEC_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -170,6 +196,28 @@ int spec_verify_greedy(const spec_batch *batch, const spec_outputs *out, void *w
         return SPEC_ERR_WORKSPACE;
     VerifyParams p = base_params(batch, out, workspace, false);
     return run_verify(MODE_GREEDY, batch, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int spec_verify_greedy_noalloc(const spec_batch *batch, const spec_outputs *out, spec_stream stream)
+{
+    int rc = check_batch(batch, out);
+    if (rc != SPEC_OK) return rc;
+    const int elt = static_cast<int>(elt_bytes(batch->dtype));
+    if (ws_bytes(batch->R_cap, batch->B, batch->V, elt, false) > SPEC_NOALLOC_SCRATCH_BYTES)
+        return SPEC_ERR_WORKSPACE;
+    void *ws = nullptr;
+    rc = noalloc_scratch(&ws);
+    if (rc != SPEC_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the per-request and per-row tickets must start at zero (they are
+    // adjacent in the layout); the rest is written before it is read
+    const WsLayout l = ws_layout(ws, batch->R_cap, batch->B, batch->V, elt, false);
+    const size_t tick = align256(static_cast<size_t>(batch->B) * 4) +
+                        align256(static_cast<size_t>(batch->R_cap) * 4);
+    cudaError_t e = cudaMemsetAsync(l.ticket, 0, tick, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    VerifyParams p = base_params(batch, out, ws, false);
+    return run_verify(MODE_GREEDY, batch, p, s);
 }
 
 int spec_verify_relaxed_topk(const spec_batch *batch, const int32_t *relaxed_k,
