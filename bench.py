@@ -42,6 +42,10 @@ KERNEL_SOURCES = ["speculative_decoding_verification_ragged_gb300/csrc/verify.cu
                   "speculative_decoding_verification_ragged_gb300/csrc/common.cuh"]
 
 
+# kernels one spec_verify_sample call launches: prologue, stream, finish, heavy
+LAUNCHES_PER_CALL = 4
+
+
 def kernel_digest() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -151,6 +155,7 @@ def run_ours(args) -> None:
 
     import speculative_decoding_verification_ragged_gb300 as sv
     import speculative_decoding_verification_ragged_gb300.binding  # noqa: F401
+    from speculative_decoding_verification_ragged_gb300 import shard
     sv.build()
 
     vb, p = make_inputs(W.data_seed(3) + rank)
@@ -203,10 +208,7 @@ def run_ours(args) -> None:
     total_ms = t0.elapsed_time(t1)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     mean_launch_ms = sum(launch_ms) / len(launch_ms)
-    if world > 1:
-        tt_ = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt_, op=dist.ReduceOp.MAX)
-        total_ms = float(tt_.item())
+    total_ms = shard.max_over_ranks(total_ms, dev)          # the job's time: its slowest rank
 
     # end to end through the public API with host buffers: H2D of the step's
     # inputs from pinned memory, the call, D2H of the step's results
@@ -243,10 +245,9 @@ def run_ours(args) -> None:
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt_ = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt_, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt_.item())
+    e2e_ms = shard.max_over_ranks(e2e_ms, dev)
+    # job-wide prefix-acceptance counters (one sum all-reduce, at read time)
+    shard.reduce_prefix_stats(acc, ver, hist)
 
     entries = time_entry_points(sv, dev, stream, args) if (rank == 0 and not args.no_entries) else None
 
@@ -281,12 +282,15 @@ def run_ours(args) -> None:
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "traffic": traffic_record(), "peak_source": peaks["source"],
-                         "kernel": "verify_rows_kernel<bf16, sample>",
+                         "kernel": "spec_verify_sample call (row_info + stream_chunks + "
+                                   "finish_rows + heavy_rows kernels, bf16)",
                          "algorithmic_bytes_per_launch": bytes_per_launch,
                          "mean_launch_us": round(mean_launch_ms * 1e3, 3)},
             "e2e": {"value": round(world * R * e2e_steps / (e2e_ms * 1e-3), 1), "unit": "rows/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": args.steps,
+            "gpu_launches": LAUNCHES_PER_CALL * args.steps,
+            "prefix_acceptance": [round(float(x), 4) for x in
+                                  shard.prefix_acceptance(acc.cpu().numpy(), ver.cpu().numpy())],
             "clocks": clocks.summary(),
         }
         if entries is not None:
@@ -301,26 +305,37 @@ def run_ours(args) -> None:
 
 
 def _time_launches(fn, n: int, stream) -> float:
-    """Mean device time (ms) of fn() over n launches, events on `stream`."""
+    """Mean device time (ms) of fn(i) over n back-to-back launches: the GPU
+    is kept busy while the host queues them, then one pair of events on
+    `stream` brackets the n calls."""
     import torch
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n)]
-    torch.cuda._sleep(100_000_000)   # keep the GPU busy while the host queues the launches
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(100_000_000)
+    t0.record(stream)
     for i in range(n):
-        ev[i][0].record(stream)
         fn(i)
-        ev[i][1].record(stream)
+    t1.record(stream)
     torch.cuda.synchronize()
-    return sum(a.elapsed_time(b) for a, b in ev) / n
+    return t0.elapsed_time(t1) / n
 
 
 def time_entry_points(sv, dev, stream, args) -> dict:
     """Device time of the other entry points at their workload shapes
-    (inputs rotate over device copies larger than L2)."""
+    (inputs rotate over device copies larger than L2).  Arguments are
+    marshalled once; each timed launch is one C-ABI call."""
+    import ctypes as C
     import torch
+    from speculative_decoding_verification_ragged_gb300 import binding as Bd
+
+    L = Bd.load_library()
+    s = stream.cuda_stream
 
     def bf(x):
         return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def ok(rc):
+        if rc:
+            raise RuntimeError("entry point returned %d" % rc)
 
     out = {}
     n = args.entry_launches
@@ -329,13 +344,17 @@ def time_entry_points(sv, dev, stream, args) -> dict:
     sets = [bf(vb.logits) for _ in range(args.sets)]
     cu, dr = torch.from_numpy(vb.cu_rows).to(dev), torch.from_numpy(vb.draft_ids).to(dev)
     ws = sv.new_workspace(vb.R, vb.B, vb.V, torch.bfloat16, dev)
-    fn = lambda i: sv.verify_greedy(sets[i % len(sets)], cu, dr, V=vb.V, B=vb.B, k_max=vb.k_max,
-                                    R_cap=vb.R, workspace=ws, rows=True, stream=stream)
+    b = Bd._batch(sets[0], vb.V, vb.B, vb.k_max, vb.R, cu, dr)
+    o, _ = Bd._outputs(vb.B, vb.k_max, vb.R, dev, True, None)
+
+    def greedy(i):
+        b.logits = sets[i % len(sets)].data_ptr()
+        ok(L.spec_verify_greedy(C.byref(b), C.byref(o), ws.data_ptr(), ws.numel(), s))
     for i in range(5):
-        fn(i)
-    ms = _time_launches(fn, n, stream)
-    out["spec_verify_greedy"] = {"workload": "B=128 k=4 V=152064 bf16 planted", "rows": vb.R,
-                                 "us": round(ms * 1e3, 2),
+        greedy(i)
+    ms = _time_launches(greedy, n, stream)
+    out["spec_verify_greedy"] = {"workload": "B=128 k=4 V=152064 bf16 planted, with row max/LSE/argmax",
+                                 "rows": vb.R, "us": round(ms * 1e3, 2),
                                  "hbm_gbs": round(vb.R * vb.V * 2 / (ms * 1e-3) / 1e9, 1)}
     del sets
     # relaxed top-K (EAGLE-relaxed, B=256, k=5, V=152064, K=4)
@@ -346,12 +365,16 @@ def time_entry_points(sv, dev, stream, args) -> dict:
     ws = sv.new_workspace(vb.R, vb.B, vb.V, torch.bfloat16, dev)
     acc = torch.zeros(vb.k_max, dtype=torch.int64, device=dev)
     ver, hist = acc.clone(), torch.zeros(vb.k_max + 1, dtype=torch.int64, device=dev)
-    fn = lambda i: sv.verify_relaxed_topk(sets[i % 2], cu, dr, K, V=vb.V, B=vb.B, k_max=vb.k_max,
-                                          R_cap=vb.R, workspace=ws, rows=True,
-                                          stats=(acc, ver, hist), stream=stream)
+    b = Bd._batch(sets[0], vb.V, vb.B, vb.k_max, vb.R, cu, dr)
+    o, _ = Bd._outputs(vb.B, vb.k_max, vb.R, dev, True, (acc, ver, hist))
+
+    def relaxed(i):
+        b.logits = sets[i % 2].data_ptr()
+        ok(L.spec_verify_relaxed_topk(C.byref(b), K.data_ptr(), C.byref(o), ws.data_ptr(),
+                                      ws.numel(), s))
     for i in range(5):
-        fn(i)
-    ms = _time_launches(fn, n, stream)
+        relaxed(i)
+    ms = _time_launches(relaxed, n, stream)
     out["spec_verify_relaxed_topk"] = {"workload": "B=256 k=5 V=152064 bf16 K=4 + fused stats",
                                        "rows": vb.R, "us": round(ms * 1e3, 2),
                                        "hbm_gbs": round(vb.R * vb.V * 2 / (ms * 1e-3) / 1e9, 1)}
@@ -359,23 +382,35 @@ def time_entry_points(sv, dev, stream, args) -> dict:
     # draft confidence + allocation (MTP/DSpark-shaped, B=16, k=7, V=151552)
     db = W.mtp_adaptive(planted_draft=True)
     dsets = [bf(db.draft_logits) for _ in range(8)]
-    dws = sv.binding.new_draft_workspace(db.B, db.k, db.V, torch.bfloat16, dev)
-    fn = lambda i: sv.draft_confidence(dsets[i % 8], V=db.V, B=db.B, k=db.k, threshold=0.3,
-                                       workspace=dws, stream=stream)
+    dws = Bd.new_draft_workspace(db.B, db.k, db.V, torch.bfloat16, dev)
+    d = Bd.Draft(dsets[0].data_ptr(), Bd.SPEC_BF16, db.V, dsets[0].stride(0), db.B, db.k, None,
+                 0.3, 0)
+    cap = db.B * (db.k + 1)
+    bufs = [torch.empty(db.B * db.k, dtype=torch.float32, device=dev)] + \
+           [torch.empty(x, dtype=torch.int32, device=dev)
+            for x in [db.B * db.k, db.B, db.B + 1, cap, cap, cap, 1, 1]]
+    a = Bd.Allocation(*[t.data_ptr() for t in bufs])
+
+    def conf(i):
+        d.draft_logits = dsets[i % 8].data_ptr()
+        ok(L.spec_draft_confidence(C.byref(d), C.byref(a), dws.data_ptr(), dws.numel(), s))
     for i in range(5):
-        fn(i)
-    ms = _time_launches(fn, n, stream)
+        conf(i)
+    ms = _time_launches(conf, n, stream)
     rows = db.B * db.k
     out["spec_draft_confidence"] = {"workload": "B=16 k=7 V=151552 bf16, threshold 0.3",
                                     "rows": rows, "us": round(ms * 1e3, 2),
                                     "hbm_gbs": round(rows * db.V * 2 / (ms * 1e-3) / 1e9, 1)}
     # standalone prefix statistics
-    a = torch.randint(0, 5, (128,), dtype=torch.int32, device=dev)
+    al = torch.randint(0, 5, (128,), dtype=torch.int32, device=dev)
     cu = torch.arange(0, 129 * 5, 5, dtype=torch.int32, device=dev)
     acc = torch.zeros(4, dtype=torch.int64, device=dev)
     ver, hist = acc.clone(), torch.zeros(5, dtype=torch.int64, device=dev)
-    fn = lambda i: sv.prefix_stats(a, cu, acc, ver, hist, B=128, k_max=4, stream=stream)
-    ms = _time_launches(fn, n, stream)
+
+    def stats(i):
+        ok(L.spec_prefix_stats(al.data_ptr(), cu.data_ptr(), 128, 4, acc.data_ptr(), ver.data_ptr(),
+                               hist.data_ptr(), None, s))
+    ms = _time_launches(stats, n, stream)
     out["spec_prefix_stats"] = {"workload": "B=128 k=4", "us": round(ms * 1e3, 2), "hbm_gbs": 0.0}
     return out
 
