@@ -102,6 +102,7 @@ struct __align__(16) ChunkPart {
     float lev;      // sampler with a bound: the level the candidates lie above
 };
 static_assert(sizeof(ChunkPart) == 32, "chunk summary is 32 bytes");
+static_assert(kChunkBytes / 16 <= 32 * kThreads, "a thread's vectors of a chunk fit a 32-bit mask");
 static_assert(2 * kRowStage <= kChunkBytes, "the heavy kernel streams rows through its chunk buffer");
 
 // Record of a row queued for the heavy kernel (32 bytes, at the start of the
@@ -666,12 +667,14 @@ __global__ void __launch_bounds__(256) row_info_kernel(const VerifyParams p, int
 // ------------------------------------------------------ stream kernel ----
 
 // Exact k-th largest of the CTA's thread maxima (k <= kThreads): at least k
-// distinct elements of the chunk are >= it.  A radix select over the 256
-// values whose first digit starts at the highest key bit where their minimum
-// and maximum differ.
+// distinct elements of the chunk are >= it.  A bitwise search on the values'
+// order-preserving keys: below the bits the minimum and maximum share, each
+// bit is kept when at least k keys reach the prefix with it set (one
+// barrier count per bit, no histogram).
 template <typename E>
 __device__ __forceinline__ float kth_thread_max(float v, int k, float m_c, Shared &sh)
 {
+    constexpr int VS = (E::BYTES == 2) ? 16 : 0;
     float mn = v;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
@@ -680,11 +683,17 @@ __device__ __forceinline__ float kth_thread_max(float v, int k, float m_c, Share
     float lo = INFINITY;
     for (int w = 0; w < kWarps; ++w) lo = fminf(lo, sh.red_f[w]);
     __syncthreads();
-    auto visit = [&](auto &&fn, float thr) {
-        if (v >= thr) fn(v, 0);
-    };
-    const uint32_t key = select_key<E, false>(visit, fkey(lo), fkey(m_c), 0.f,
-                                              static_cast<uint32_t>(k), 0.f, 0.f, sh);
+    const uint32_t mine = fkey(v) >> VS;
+    const uint32_t klo = fkey(lo) >> VS, khi = fkey(m_c) >> VS;
+    const uint32_t x = klo ^ khi;
+    const int top = x ? 31 - __clz(x) : -1;
+    // every key lies in [klo, khi]: the bits above `top` are theirs
+    uint32_t ans = (top >= 31) ? 0u : (khi >> (top + 1)) << (top + 1);
+    for (int bit = top; bit >= 0; --bit) {
+        const uint32_t cand = ans | (1u << bit);
+        if (__syncthreads_count(mine >= cand) >= k) ans = cand;
+    }
+    const uint32_t key = VS ? ((ans << 16) | ((ans & 0x8000u) ? 0u : 0xFFFFu)) : ans;
     return key_floor(key);
 }
 
@@ -903,10 +912,52 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 4 : 6)
             if (bounded) {
                 if (tid == 0) sh.cand_n = 0;
                 __syncthreads();
-                visit_chunk([&](float v, int32_t ix) {
-                    const int slot = warp_append(&sh.cand_n);
-                    if (slot < kCandCap) { cand[slot].v = v; cand[slot].i = ix; }
-                }, lo);
+                // count this thread's elements >= lo and remember which of
+                // its vectors hold them (compares only), reserve a range per
+                // warp with one atomic, then re-read just those vectors
+                uint32_t hits = 0;
+                int cnt = 0;
+                for (int i = tid, j = 0; i < g.nb; i += kThreads, ++j) {
+                    const uint4 v = body[i];
+                    if (!(E::vmax(v) >= lo)) continue;
+                    float x[VEC];
+                    E::unpack(v, x);
+                    int cv = 0;
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) cv += (x[q] >= lo) ? 1 : 0;
+                    cnt += cv;
+                    hits |= (cv ? 1u : 0u) << j;
+                }
+                const bool xin = tid < g.n_extra && sh.extras_v[tid] >= lo;
+                cnt += xin ? 1 : 0;
+                int off = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xFFFFFFFFu, off, o);
+                    if (lane >= o) off += y;
+                }
+                int base = 0;
+                if (lane == 31 && off) base = atomicAdd(&sh.cand_n, off);
+                base = __shfl_sync(0xFFFFFFFFu, base, 31);
+                off += base - cnt;
+                while (hits) {
+                    const int j = __ffs(hits) - 1;
+                    hits &= hits - 1;
+                    const int i = tid + j * kThreads;
+                    const uint4 v = body[i];
+                    float x[VEC];
+                    E::unpack(v, x);
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q)
+                        if (x[q] >= lo) {
+                            if (off < kCandCap) { cand[off].v = x[q]; cand[off].i = g.a0 + i * VEC + q; }
+                            ++off;
+                        }
+                }
+                if (xin) {
+                    if (off < kCandCap) { cand[off].v = sh.extras_v[tid]; cand[off].i = sh.extras_i[tid]; }
+                    ++off;
+                }
                 __syncthreads();
                 n = sh.cand_n;
                 Cand *ws_list = reinterpret_cast<Cand *>(p.ws_cand) + rc * kCandCap;
