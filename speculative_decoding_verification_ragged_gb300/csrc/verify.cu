@@ -457,8 +457,18 @@ __device__ __forceinline__ int32_t abs_bin(float z, float s8)
 // keys of the floats from -inf to +inf.
 __device__ __forceinline__ float bin_floor_value(int32_t q, float s8)
 {
-    uint32_t lo = fkey(-INFINITY), hi = fkey(INFINITY);   // abs_bin(+inf) is the largest bin
     if (abs_bin(-INFINITY, s8) >= q) return -INFINITY;
+    // the answer lies within a few floats of q / s8: walk there first
+    {
+        uint32_t k = fkey(static_cast<float>(q) / s8);
+        for (int it = 0; it < 16; ++it) {
+            if (k <= fkey(-INFINITY) || k >= fkey(INFINITY)) break;
+            const bool in = abs_bin(key_value(k), s8) >= q;
+            if (in && abs_bin(key_value(k - 1), s8) < q) return key_value(k);
+            k = in ? k - 1 : k + 1;
+        }
+    }
+    uint32_t lo = fkey(-INFINITY), hi = fkey(INFINITY);   // abs_bin(+inf) is the largest bin
     while (hi - lo > 1) {
         const uint32_t mid = lo + (hi - lo) / 2;
         if (abs_bin(key_value(mid), s8) >= q) hi = mid;
@@ -1271,14 +1281,28 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
             const int n_list = sh.total;
             const bool staged = !sh.overflow && n_list <= kListCap;
             auto stage_lists = [&]() {
+                // n_list <= kListCap: at most kListCap / kThreads entries per
+                // thread, all loads issued before any is used
+                constexpr int PER = kListCap / kThreads;
                 const float2 *wl = reinterpret_cast<const float2 *>(p.ws_cand) +
                                    static_cast<int64_t>(r) * nchunk * kCandCap;
-                for (int e = tid; e < n_list; e += kThreads) {
-                    int q = 0;
-                    while (sh.offs[q + 1] <= e) ++q;
-                    const float2 v = __ldcg(wl + static_cast<int64_t>(q) * kCandCap + (e - sh.offs[q]));
-                    lst[e].v = v.x;
-                    lst[e].i = __float_as_int(v.y);
+                float2 v[PER];
+#pragma unroll
+                for (int u = 0; u < PER; ++u) {
+                    const int e = tid + u * kThreads;
+                    if (e < n_list) {
+                        int q = 0;
+                        while (sh.offs[q + 1] <= e) ++q;
+                        v[u] = __ldcg(wl + static_cast<int64_t>(q) * kCandCap + (e - sh.offs[q]));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < PER; ++u) {
+                    const int e = tid + u * kThreads;
+                    if (e < n_list) {
+                        lst[e].v = v[u].x;
+                        lst[e].i = __float_as_int(v[u].y);
+                    }
                 }
                 __syncthreads();
             };
@@ -1325,14 +1349,22 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
                 if (!heavy) {
                     // combined mass of absolute bin J - t, then C(t) = mass of
                     // bins J - t .. J (thread t)
+                    // the row's bins staged in shared memory by all threads
+                    // at once (the band and list scratch, 32 KiB, holds 64
+                    // chunks of them)
+                    float *sb = reinterpret_cast<float *>(band);
+                    {
+                        const float *rb = p.ws_bins + static_cast<int64_t>(r) * nchunk * kBins;
+#pragma unroll 4
+                        for (int i = tid; i < nchunk * kBins; i += kThreads) sb[i] = __ldcg(rb + i);
+                    }
+                    __syncthreads();
                     float hb = 0.f;
                     if (tid < kBins) {
-                        const float *rb = p.ws_bins + static_cast<int64_t>(r) * nchunk * kBins;
                         for (int q = 0; q < nchunk; ++q) {
                             if (!(parts[q].m > -INFINITY)) continue;
                             const int tq = tid - (J - parts[q].gidx);
-                            if (tq >= 0 && tq < kBins)
-                                hb += __ldcg(rb + q * kBins + tq) * ex2((parts[q].m - M) * sc);
+                            if (tq >= 0 && tq < kBins) hb += sb[q * kBins + tq] * ex2((parts[q].m - M) * sc);
                         }
                     }
                     float cum = hb;
@@ -1582,77 +1614,85 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
             float mass = 0.f, best = -INFINITY;
             int32_t bi = INT_MAX;
             const uint4 *body = reinterpret_cast<const uint4 *>(chunk);
-            // count this thread's nucleus (z >= zin) and band (zband <= z <
-            // zin) values: compares only
-            int ns = 0, nbd = 0;
-            for (int i = tid; i < g.nb; i += kThreads) {
+            // count this thread's values >= zband (one compare each) and mark
+            // the vectors that hold them; a CTA scan gives each thread its
+            // range of `sure`; the marked vectors are read again to scatter
+            uint32_t hits = 0;
+            int cnt = 0;
+            for (int i = tid, j = 0; i < g.nb; i += kThreads, ++j) {
                 const uint4 v = body[i];
                 if (!(E::vmax(v) >= zband)) continue;
                 float x[VEC];
                 E::unpack(v, x);
+                int cv = 0;
 #pragma unroll
-                for (int q = 0; q < VEC; ++q) {
-                    ns += (x[q] >= zin) ? 1 : 0;
-                    nbd += (x[q] >= zband && !(x[q] >= zin)) ? 1 : 0;
-                }
+                for (int q = 0; q < VEC; ++q) cv += (x[q] >= zband) ? 1 : 0;
+                cnt += cv;
+                hits |= (cv ? 1u : 0u) << j;
             }
-            if (tid < g.n_extra) {
-                ns += (xe >= zin) ? 1 : 0;
-                nbd += (xe >= zband && !(xe >= zin)) ? 1 : 0;
-            }
-            // exclusive offsets of both counts across the CTA
-            int os = ns, ob = nbd;
+            const bool xin = tid < g.n_extra && xe >= zband;
+            cnt += xin ? 1 : 0;
+            int off = cnt;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int a1 = __shfl_up_sync(0xFFFFFFFFu, os, o);
-                const int b1 = __shfl_up_sync(0xFFFFFFFFu, ob, o);
-                if (lane >= o) { os += a1; ob += b1; }
+                const int y = __shfl_up_sync(0xFFFFFFFFu, off, o);
+                if (lane >= o) off += y;
             }
-            if (lane == 31) { sh.red_i[warp] = os; sh.red_i[kWarps + warp] = ob; }
+            if (lane == 31) sh.red_i[warp] = off;
+            if (tid == 0) sh.total = 0;
             __syncthreads();
-            int ws = 0, wb = 0, ts = 0, tb = 0;
+            int tot = 0;
             for (int w = 0; w < kWarps; ++w) {
-                if (w < warp) { ws += sh.red_i[w]; wb += sh.red_i[kWarps + w]; }
-                ts += sh.red_i[w];
-                tb += sh.red_i[kWarps + w];
+                if (w < warp) off += sh.red_i[w];
+                tot += sh.red_i[w];
             }
-            os += ws - ns;
-            ob += wb - nbd;
-            // scatter: nucleus values to `sure` (scored directly past its
-            // capacity), band values to `band`
+            off -= cnt;
+            // values past the buffer's capacity are handled on the spot
             auto place = [&](float v, int32_t ix) {
-                if (v >= zin) {
-                    if (os < kSureCap) { sure[os].v = v; sure[os].i = ix; }
-                    else { mass += ex2((v - M) * sc); keep_best(nz.score(v, ix, f.invT), ix, best, bi); }
-                    ++os;
-                } else if (v >= zband) {
-                    if (ob < kCandCap) { band[ob].v = v; band[ob].i = ix; }
-                    ++ob;
+                if (off < kSureCap) {
+                    sure[off].v = v;
+                    sure[off].i = ix;
+                } else if (v >= zin) {
+                    mass += ex2((v - M) * sc);
+                    keep_best(nz.score(v, ix, f.invT), ix, best, bi);
+                } else {
+                    const int slot = warp_append(&sh.total);
+                    if (slot < kCandCap) { band[slot].v = v; band[slot].i = ix; }
                 }
+                ++off;
             };
-            if (ns + nbd > 0) {
-                for (int i = tid; i < g.nb; i += kThreads) {
-                    const uint4 v = body[i];
-                    if (!(E::vmax(v) >= zband)) continue;
-                    float x[VEC];
-                    E::unpack(v, x);
+            while (hits) {
+                const int j = __ffs(hits) - 1;
+                hits &= hits - 1;
+                const int i = tid + j * kThreads;
+                const uint4 v = body[i];
+                float x[VEC];
+                E::unpack(v, x);
 #pragma unroll
-                    for (int q = 0; q < VEC; ++q) place(x[q], g.a0 + i * VEC + q);
+                for (int q = 0; q < VEC; ++q)
+                    if (x[q] >= zband) place(x[q], g.a0 + i * VEC + q);
+            }
+            if (xin) place(xe, ie);
+            __syncthreads();
+            // the collected values with all lanes busy: nucleus values add
+            // their mass and their Gumbel score, band values go to the band
+            const int n_sel = min(tot, kSureCap);
+            for (int i = tid; i < n_sel; i += kThreads) {
+                const Cand e = sure[i];
+                if (e.v >= zin) {
+                    mass += ex2((e.v - M) * sc);
+                    keep_best(nz.score(e.v, e.i, f.invT), e.i, best, bi);
+                } else {
+                    const int slot = warp_append(&sh.total);
+                    if (slot < kCandCap) { band[slot].v = e.v; band[slot].i = e.i; }
                 }
-                if (tid < g.n_extra) place(xe, ie);
             }
             __syncthreads();
             // the chunk's band values to its own list (no global atomics)
+            const int tb = sh.total;
             float2 *clist = blist + static_cast<int64_t>(c) * kCandCap;
             for (int i = tid; i < min(tb, kCandCap); i += kThreads)
                 clist[i] = make_float2(band[i].v, __int_as_float(band[i].i));
-            // the compacted nucleus values: mass and scores with all lanes busy
-            const int n_sure = min(ts, kSureCap);
-            for (int i = tid; i < n_sure; i += kThreads) {
-                const Cand e = sure[i];
-                mass += ex2((e.v - M) * sc);
-                keep_best(nz.score(e.v, e.i, f.invT), e.i, best, bi);
-            }
             block_best(best, bi, sh);
             mass = block_sum(mass, sh);
             if (tid == 0) {
@@ -1673,12 +1713,16 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
             __syncthreads();
             if (sh.last) {
                 // ---- the row's last chunk: settle the band ----
+                // the row's chunk results, loaded by one thread each
+                float4 *hps = reinterpret_cast<float4 *>(band);
+                if (tid < nchunk)
+                    hps[tid] = __ldcg(reinterpret_cast<const float4 *>(reinterpret_cast<const HeavyPart *>(area + 8) + tid));
+                __syncthreads();
                 if (tid == 0) {
-                    const HeavyPart *hp = reinterpret_cast<const HeavyPart *>(area + 8);
                     float bsum = 0.f, bb = -INFINITY;
                     int32_t bbi = INT_MAX, tot = 0, ovf = 0;
                     for (int q = 0; q < nchunk; ++q) {
-                        const float4 e = __ldcg(reinterpret_cast<const float4 *>(hp + q));
+                        const float4 e = hps[q];
                         bsum += e.z;
                         keep_best(e.x, __float_as_int(e.y), bb, bbi);
                         const int nq = __float_as_int(e.w);
