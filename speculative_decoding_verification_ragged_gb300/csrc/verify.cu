@@ -1647,20 +1647,9 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                 tot += sh.red_i[w];
             }
             off -= cnt;
-            // values past the buffer's capacity are handled on the spot
-            auto place = [&](float v, int32_t ix) {
-                if (off < kSureCap) {
-                    sure[off].v = v;
-                    sure[off].i = ix;
-                } else if (v >= zin) {
-                    mass += ex2((v - M) * sc);
-                    keep_best(nz.score(v, ix, f.invT), ix, best, bi);
-                } else {
-                    const int slot = warp_append(&sh.total);
-                    if (slot < kCandCap) { band[slot].v = v; band[slot].i = ix; }
-                }
-                ++off;
-            };
+            // scatter into `sure` up to its capacity (a plain store per value)
+            const uint32_t hits0 = hits;
+            const int off0 = off;
             while (hits) {
                 const int j = __ffs(hits) - 1;
                 hits &= hits - 1;
@@ -1670,9 +1659,43 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                 E::unpack(v, x);
 #pragma unroll
                 for (int q = 0; q < VEC; ++q)
-                    if (x[q] >= zband) place(x[q], g.a0 + i * VEC + q);
+                    if (x[q] >= zband) {
+                        if (off < kSureCap) { sure[off].v = x[q]; sure[off].i = g.a0 + i * VEC + q; }
+                        ++off;
+                    }
             }
-            if (xin) place(xe, ie);
+            if (xin) {
+                if (off < kSureCap) { sure[off].v = xe; sure[off].i = ie; }
+                ++off;
+            }
+            if (tot > kSureCap) {
+                // rare: the values past the buffer are handled where they are
+                auto direct = [&](float v, int32_t ix) {
+                    if (v >= zin) {
+                        mass += ex2((v - M) * sc);
+                        keep_best(nz.score(v, ix, f.invT), ix, best, bi);
+                    } else {
+                        const int slot = warp_append(&sh.total);
+                        if (slot < kCandCap) { band[slot].v = v; band[slot].i = ix; }
+                    }
+                };
+                int o2 = off0;
+                uint32_t hh = hits0;
+                while (hh) {
+                    const int j = __ffs(hh) - 1;
+                    hh &= hh - 1;
+                    const int i = tid + j * kThreads;
+                    const uint4 v = body[i];
+                    float x[VEC];
+                    E::unpack(v, x);
+                    for (int q = 0; q < VEC; ++q)
+                        if (x[q] >= zband) {
+                            if (o2 >= kSureCap) direct(x[q], g.a0 + i * VEC + q);
+                            ++o2;
+                        }
+                }
+                if (xin && o2 >= kSureCap) direct(xe, ie);
+            }
             __syncthreads();
             // the collected values with all lanes busy: nucleus values add
             // their mass and their Gumbel score, band values go to the band
