@@ -768,7 +768,7 @@ __device__ __forceinline__ void chunk_reduce(float tmax, int32_t targ, float tsu
 // One CTA per (row, chunk); plain stores of the chunk summary only.  Many
 // short CTAs per SM keep the bulk copies in flight.
 template <typename TIn, int MODE>
-__global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 4 : 6)
+__global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
     stream_chunks_kernel(const VerifyParams p)
 {
     using E = Elt<TIn>;
