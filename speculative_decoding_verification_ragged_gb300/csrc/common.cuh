@@ -171,6 +171,14 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
     return d;
 }
 
+// a + b rounded toward -inf in each half
+__device__ __forceinline__ uint64_t f2_add_rm(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // ------------------------------------------------------------ values -----
 
 // Order-preserving 32-bit key of a float; -0.0 and +0.0 map to one key.

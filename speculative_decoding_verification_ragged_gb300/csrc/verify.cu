@@ -70,6 +70,7 @@ constexpr int kCandCap = kWsCandCap;    // candidates one chunk may store
 constexpr int kBins = kWsBins;          // pure top-p mass bins per chunk
 constexpr float kBinsPerT = 8.0f;       // bin width T/8
 constexpr float kFix = 1048576.0f;      // fixed-point scale of one bin weight (2^20)
+constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: adding it leaves integer parts in the low bits
 constexpr int32_t kNoBins = INT_MIN;    // chunk grid origin too large for exact bins
 constexpr int kBandCap = 2048;          // undecided values kept on chip
 constexpr int kListCap = 2048;          // candidates the finish kernel stages on chip
@@ -986,15 +987,67 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
                 const int32_t jt = abs_bin(m_c, s8);
                 uint32_t *mine = wbins + warp * kBins;
                 float tail = 0.f;
-                visit_chunk([&](float v, int32_t) {
-                    const int32_t t = jt - abs_bin(v, s8);
-                    if (t < kBins) {
-                        const float w = ex2(fmaf(v - m_c, invT, static_cast<float>(t) * (1.0f / kBinsPerT)) * kLog2e);
-                        atomicAdd(mine + t, __float2uint_rn(fminf(w, 1.25f) * kFix));
-                    } else {
-                        tail += ex2((v - m_c) * sc);
+                if (jt >= -(1 << 21) && jt <= (1 << 21)) {
+                    // Integer parts without conversions: for |u| < 2^22,
+                    // u + 1.5*2^23 rounded down is floor(u) + 1.5*2^23, an
+                    // integer in [2^23, 2^24) whose bit pattern differs from
+                    // the constant's by floor(u).  u = z*s8 rounded as in
+                    // abs_bin, raised to jt - 2*kBins (those values land in
+                    // the tail either way), so the bin equals abs_bin(z).
+                    // The fixed-point weight uses the same trick with
+                    // round-to-nearest (w < 4 here).
+                    const float ulo = static_cast<float>(jt - 2 * kBins);
+                    const float yt = static_cast<float>(jt) + kMagic;
+                    const uint32_t ytb = __float_as_uint(yt);
+                    const uint64_t s8_2 = f2_pack(s8, s8), mg2 = f2_pack(kMagic, kMagic);
+                    const uint64_t yt2 = f2_pack(yt, yt), m1_2 = f2_pack(-1.f, -1.f);
+                    const uint64_t nm2 = f2_pack(-m_c, -m_c), sc2 = f2_pack(sc, sc);
+                    const float c8 = kLog2e / kBinsPerT;
+                    const uint64_t c8_2 = f2_pack(c8, c8);
+                    auto bin_add = [&](float w, uint32_t t) {
+                        if (t < static_cast<uint32_t>(kBins))
+                            atomicAdd(mine + t, __float_as_uint(fmaf(w, kFix, kMagic)) - __float_as_uint(kMagic));
+                        else
+                            tail += w;
+                    };
+                    auto bin_pair = [&](uint64_t xx) {
+                        float u0, u1;
+                        f2_unpack(f2_mul(xx, s8_2), u0, u1);
+                        const uint64_t y = f2_add_rm(f2_pack(fmaxf(u0, ulo), fmaxf(u1, ulo)), mg2);
+                        const uint64_t ds = f2_mul(f2_add(xx, nm2), sc2);
+                        const uint64_t in = f2_fma(f2_fma(y, m1_2, yt2), c8_2, ds);
+                        float y0, y1, a0, a1, b0, b1;
+                        f2_unpack(y, y0, y1);
+                        f2_unpack(in, a0, a1);
+                        f2_unpack(ds, b0, b1);
+                        const uint32_t t0 = ytb - __float_as_uint(y0), t1 = ytb - __float_as_uint(y1);
+                        bin_add(ex2(t0 < static_cast<uint32_t>(kBins) ? a0 : b0), t0);
+                        bin_add(ex2(t1 < static_cast<uint32_t>(kBins) ? a1 : b1), t1);
+                    };
+                    for (int i = tid; i < g.nb; i += kThreads) {
+                        const uint4 v = body[i];
+                        if constexpr (E::BYTES == 2) {
+                            bin_pair(f2_pack(bf_lo(v.x), bf_hi(v.x)));
+                            bin_pair(f2_pack(bf_lo(v.y), bf_hi(v.y)));
+                            bin_pair(f2_pack(bf_lo(v.z), bf_hi(v.z)));
+                            bin_pair(f2_pack(bf_lo(v.w), bf_hi(v.w)));
+                        } else {
+                            bin_pair(f2_pack(__uint_as_float(v.x), __uint_as_float(v.y)));
+                            bin_pair(f2_pack(__uint_as_float(v.z), __uint_as_float(v.w)));
+                        }
                     }
-                }, -INFINITY);
+                    if (tid < g.n_extra) {
+                        const float xv = sh.extras_v[tid];
+                        const float y0 = __fadd_rd(fmaxf(xv * s8, ulo), kMagic);
+                        const uint32_t t0 = ytb - __float_as_uint(y0);
+                        const float d = (xv - m_c) * sc;
+                        bin_add(ex2(t0 < static_cast<uint32_t>(kBins) ? fmaf(yt - y0, c8, d) : d), t0);
+                    }
+                } else {
+                    // no bin resolution at this grid origin: the chunk's
+                    // mass only (the combine treats the row as binless)
+                    visit_chunk([&](float v, int32_t) { tail += ex2((v - m_c) * sc); }, -INFINITY);
+                }
                 __syncthreads();
                 float mass = 0.f;
                 if (tid < kBins) {
