@@ -783,8 +783,19 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nchunk = p.nchunk;
-    const int r = static_cast<int>(blockIdx.x) / nchunk;
-    const int c = static_cast<int>(blockIdx.x) - r * nchunk;
+    // The sampler takes chunk-major order (CTA b: chunk b / rows of row
+    // b % rows): a chunk's cost depends on its row's filters, and this
+    // spreads every row's chunks evenly over the grid, with the short tail
+    // chunks in the last wave.  Uniform modes keep row-major order.
+    int r, c;
+    if (MODE == MODE_SAMPLE) {
+        const int rows = static_cast<int>(gridDim.x) / nchunk;
+        c = static_cast<int>(blockIdx.x) / rows;
+        r = static_cast<int>(blockIdx.x) - c * rows;
+    } else {
+        r = static_cast<int>(blockIdx.x) / nchunk;
+        c = static_cast<int>(blockIdx.x) - r * nchunk;
+    }
     const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
     const ChunkGeom g = chunk_geom<E>(row, c, p.V);
 
