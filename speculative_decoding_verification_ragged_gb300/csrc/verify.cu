@@ -937,18 +937,18 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
                 // count this thread's elements >= lo and remember which of
                 // its vectors hold them (compares only), reserve a range per
                 // warp with one atomic, then re-read just those vectors
+                // (the vectors are screened first and only the few that
+                // hold candidates are unpacked: a fused loop keeps the
+                // rare per-element work on every iteration)
                 uint32_t hits = 0;
+                for (int i = tid, j = 0; i < g.nb; i += kThreads, ++j)
+                    hits |= ((E::vmax(body[i]) >= lo) ? 1u : 0u) << j;
                 int cnt = 0;
-                for (int i = tid, j = 0; i < g.nb; i += kThreads, ++j) {
-                    const uint4 v = body[i];
-                    if (!(E::vmax(v) >= lo)) continue;
+                for (uint32_t hh = hits; hh; hh &= hh - 1) {
                     float x[VEC];
-                    E::unpack(v, x);
-                    int cv = 0;
+                    E::unpack(body[tid + (__ffs(hh) - 1) * kThreads], x);
 #pragma unroll
-                    for (int q = 0; q < VEC; ++q) cv += (x[q] >= lo) ? 1 : 0;
-                    cnt += cv;
-                    hits |= (cv ? 1u : 0u) << j;
+                    for (int q = 0; q < VEC; ++q) cnt += (x[q] >= lo) ? 1 : 0;
                 }
                 const bool xin = tid < g.n_extra && sh.extras_v[tid] >= lo;
                 cnt += xin ? 1 : 0;
@@ -1682,17 +1682,14 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
             // the vectors that hold them; a CTA scan gives each thread its
             // range of `sure`; the marked vectors are read again to scatter
             uint32_t hits = 0;
+            for (int i = tid, j = 0; i < g.nb; i += kThreads, ++j)
+                hits |= ((E::vmax(body[i]) >= zband) ? 1u : 0u) << j;
             int cnt = 0;
-            for (int i = tid, j = 0; i < g.nb; i += kThreads, ++j) {
-                const uint4 v = body[i];
-                if (!(E::vmax(v) >= zband)) continue;
+            for (uint32_t hh = hits; hh; hh &= hh - 1) {
                 float x[VEC];
-                E::unpack(v, x);
-                int cv = 0;
+                E::unpack(body[tid + (__ffs(hh) - 1) * kThreads], x);
 #pragma unroll
-                for (int q = 0; q < VEC; ++q) cv += (x[q] >= zband) ? 1 : 0;
-                cnt += cv;
-                hits |= (cv ? 1u : 0u) << j;
+                for (int q = 0; q < VEC; ++q) cnt += (x[q] >= zband) ? 1 : 0;
             }
             const bool xin = tid < g.n_extra && xe >= zband;
             cnt += xin ? 1 : 0;

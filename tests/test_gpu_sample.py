@@ -185,6 +185,24 @@ def test_pure_top_p_paths(T, tp, sigma, shift, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_pure_top_p_rows_not_vector_aligned(dtype):
+    """Diffuse nuclei in rows whose start is not 16-byte aligned: the second
+    pass over the row covers the unaligned head and tail by plain loads."""
+    sv = need_gpu()
+    V = 152064 if dtype == "bf16" else 60000
+    vb = W.ragged_batch(seed=43, B=5, k_max=3, V=V, dtype=dtype, ld=V + 3)
+    check(sv, vb, params(vb.B, 1.0, 0, 0.9, 0.0, seed=5))
+
+
+def test_many_diffuse_rows():
+    """Every row's nucleus is diffuse, and the queued rows' chunks outnumber
+    the heavy kernel's CTAs: each CTA takes several chunks of several rows."""
+    sv = need_gpu()
+    vb = W.ragged_batch(seed=47, B=80, k_max=4, V=152064, dtype="bf16")
+    check(sv, vb, params(vb.B, 1.0, 0, 0.9, 0.0, seed=9))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_unfiltered_rows_not_block_aligned(dtype):
     """Rows whose aligned body does not start on a Philox block (odd leading
     dimension): per-element noise instead of whole-vector blocks."""
