@@ -677,33 +677,45 @@ __global__ void __launch_bounds__(256) row_info_kernel(const VerifyParams p, int
 
 // ------------------------------------------------------ stream kernel ----
 
-// Exact k-th largest of the CTA's thread maxima (k <= kThreads): at least k
-// distinct elements of the chunk are >= it.  A bitwise search on the values'
-// order-preserving keys: below the bits the minimum and maximum share, each
-// bit is kept when at least k keys reach the prefix with it set (one
-// barrier count per bit, no histogram).
+// The k-th largest of the CTA's thread maxima (k <= kThreads): at least k
+// distinct elements of the chunk are >= it.  The maxima's order-preserving
+// keys go to shared memory; warp 0 holds eight each and searches bit by bit
+// below the bits the smallest and largest share, keeping a bit when at least
+// k keys reach the prefix with it set (a warp sum per bit, no CTA barrier).
 template <typename E>
 __device__ __forceinline__ float kth_thread_max(float v, int k, float m_c, Shared &sh)
 {
     constexpr int VS = (E::BYTES == 2) ? 16 : 0;
-    float mn = v;
+    (void)m_c;
+    const int lane = threadIdx.x & 31;
+    sh.hist[threadIdx.x] = fkey(v) >> VS;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        uint32_t kv[kThreads / 32];
+        uint32_t mn = 0xFFFFFFFFu, mx = 0u;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
-    if ((threadIdx.x & 31) == 0) sh.red_f[threadIdx.x >> 5] = mn;
-    __syncthreads();
-    float lo = INFINITY;
-    for (int w = 0; w < kWarps; ++w) lo = fminf(lo, sh.red_f[w]);
-    __syncthreads();
-    const uint32_t mine = fkey(v) >> VS;
-    const uint32_t klo = fkey(lo) >> VS, khi = fkey(m_c) >> VS;
-    const uint32_t x = klo ^ khi;
-    const int top = x ? 31 - __clz(x) : -1;
-    // every key lies in [klo, khi]: the bits above `top` are theirs
-    uint32_t ans = (top >= 31) ? 0u : (khi >> (top + 1)) << (top + 1);
-    for (int bit = top; bit >= 0; --bit) {
-        const uint32_t cand = ans | (1u << bit);
-        if (__syncthreads_count(mine >= cand) >= k) ans = cand;
+        for (int j = 0; j < kThreads / 32; ++j) {
+            kv[j] = sh.hist[lane + 32 * j];
+            mn = min(mn, kv[j]);
+            mx = max(mx, kv[j]);
+        }
+        mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+        const uint32_t x = mn ^ mx;
+        const int top = x ? 31 - __clz(x) : -1;
+        // every key lies in [mn, mx]: the bits above `top` are theirs
+        uint32_t ans = (top >= 31) ? 0u : (mx >> (top + 1)) << (top + 1);
+        for (int bit = top; bit >= 0; --bit) {
+            const uint32_t cand = ans | (1u << bit);
+            uint32_t c = 0;
+#pragma unroll
+            for (int j = 0; j < kThreads / 32; ++j) c += (kv[j] >= cand) ? 1u : 0u;
+            if (__reduce_add_sync(0xFFFFFFFFu, c) >= static_cast<uint32_t>(k)) ans = cand;
+        }
+        if (lane == 0) sh.sel_excl_u = ans;
     }
+    __syncthreads();
+    const uint32_t ans = sh.sel_excl_u;
     const uint32_t key = VS ? ((ans << 16) | ((ans & 0x8000u) ? 0u : 0xFFFFu)) : ans;
     return key_floor(key);
 }
