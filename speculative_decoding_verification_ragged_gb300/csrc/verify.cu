@@ -75,6 +75,7 @@ constexpr int32_t kNoBins = INT_MIN;    // chunk grid origin too large for exact
 constexpr int kBandCap = 2048;          // undecided values kept on chip
 constexpr int kListCap = 2048;          // candidates the finish kernel stages on chip
 constexpr int kSureCap = 2048;          // heavy kernel: nucleus values compacted per chunk
+constexpr int kFineBand = 64;           // heavy kernel: distinct bf16 band values tallied per chunk
 constexpr int kRowStage = 16 * 1024;    // heavy kernel: bytes per row-streaming stage
 constexpr int kPureListK = 64;          // pure top-p: list above the 64-th thread maximum
 constexpr float kMassTol = 1e-5f;       // relative slack of the bin bracket
@@ -1687,6 +1688,26 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
             const float zin = rec.zin, zband = rec.zband;
             float2 *blist = reinterpret_cast<float2 *>(p.ws_cand) +
                             static_cast<int64_t>(r) * nchunk * kCandCap;
+            // A bf16 band of at most kFineBand distinct values (keys kt - d)
+            // is tallied per value instead of listed: equal values share
+            // their weight, so a count and the best Gumbel score with its
+            // index settle the band exactly.
+            const uint32_t kt = fkey(zin) >> 16, kb = fkey(zband) >> 16;
+            const bool fine = E::BYTES == 2 && kt >= kb && kt - kb < static_cast<uint32_t>(kFineBand);
+            uint32_t *fcnt = reinterpret_cast<uint32_t *>(band);                            // [kFineBand]
+            unsigned long long *fbst = reinterpret_cast<unsigned long long *>(fcnt + kFineBand);
+            if (fine && tid < kFineBand) { fcnt[tid] = 0u; fbst[tid] = 0ull; }
+            auto band_take = [&](float v, int32_t ix) {
+                if (fine) {
+                    const uint32_t d = kt - (fkey(v) >> 16);
+                    atomicAdd(fcnt + d, 1u);
+                    atomicMax(fbst + d, (static_cast<unsigned long long>(fkey(nz.score(v, ix, f.invT))) << 32) |
+                                            static_cast<uint32_t>(~ix));
+                } else {
+                    const int slot = warp_append(&sh.total);
+                    if (slot < kCandCap) { band[slot].v = v; band[slot].i = ix; }
+                }
+            };
             float mass = 0.f, best = -INFINITY;
             int32_t bi = INT_MAX;
             const uint4 *body = reinterpret_cast<const uint4 *>(chunk);
@@ -1748,8 +1769,7 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                         mass += ex2((v - M) * sc);
                         keep_best(nz.score(v, ix, f.invT), ix, best, bi);
                     } else {
-                        const int slot = warp_append(&sh.total);
-                        if (slot < kCandCap) { band[slot].v = v; band[slot].i = ix; }
+                        band_take(v, ix);
                     }
                 };
                 int o2 = off0;
@@ -1779,16 +1799,24 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                     mass += ex2((e.v - M) * sc);
                     keep_best(nz.score(e.v, e.i, f.invT), e.i, best, bi);
                 } else {
-                    const int slot = warp_append(&sh.total);
-                    if (slot < kCandCap) { band[slot].v = e.v; band[slot].i = e.i; }
+                    band_take(e.v, e.i);
                 }
             }
             __syncthreads();
-            // the chunk's band values to its own list (no global atomics)
+            // the chunk's band values (or tallies) to its own list space (no
+            // global atomics)
             const int tb = sh.total;
             float2 *clist = blist + static_cast<int64_t>(c) * kCandCap;
-            for (int i = tid; i < min(tb, kCandCap); i += kThreads)
-                clist[i] = make_float2(band[i].v, __int_as_float(band[i].i));
+            if (fine) {
+                uint32_t *oc = reinterpret_cast<uint32_t *>(clist);
+                if (tid < kFineBand) {
+                    oc[tid] = fcnt[tid];
+                    reinterpret_cast<unsigned long long *>(oc + kFineBand)[tid] = fbst[tid];
+                }
+            } else {
+                for (int i = tid; i < min(tb, kCandCap); i += kThreads)
+                    clist[i] = make_float2(band[i].v, __int_as_float(band[i].i));
+            }
             block_best(best, bi, sh);
             mass = block_sum(mass, sh);
             if (tid == 0) {
@@ -1841,7 +1869,52 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                 const int nband = sh.total;
                 const bool ovf = sh.overflow != 0;
                 __syncthreads();
-                if (ovf || nband > kBandCap) {
+                if (fine) {
+                    // per value: the chunks' counts and best scores; the
+                    // running band mass from the top value first reaches
+                    // the target at the boundary value (all values when
+                    // rounding keeps it short); the best score among the
+                    // values down to it joins the nucleus's
+                    const float tgt = rec.target - mass_in;
+                    uint32_t n = 0;
+                    unsigned long long bb = 0ull;
+                    if (tid < kFineBand) {
+                        for (int q = 0; q < nchunk; ++q) {
+                            const uint32_t *oc = reinterpret_cast<const uint32_t *>(blist + static_cast<int64_t>(q) * kCandCap);
+                            n += __ldcg(oc + tid);
+                            bb = max(bb, __ldcg(reinterpret_cast<const unsigned long long *>(oc + kFineBand) + tid));
+                        }
+                    }
+                    float w = 0.f;
+                    if (n) {
+                        const uint32_t k = kt - static_cast<uint32_t>(tid);
+                        const float v = key_value((k << 16) | ((k & 0x8000u) ? 0u : 0xFFFFu));
+                        w = static_cast<float>(n) * ex2((v - M) * sc);
+                    }
+                    float cum = w;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float u = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+                        if (lane >= o) cum += u;
+                    }
+                    float *wt = reinterpret_cast<float *>(sh.scan);
+                    if (lane == 31) wt[warp] = cum;
+                    __syncthreads();
+                    for (int w2 = 0; w2 < warp; ++w2) cum += wt[w2];
+                    const int dstar = min(__syncthreads_count(tid < kFineBand && cum < tgt), kFineBand - 1);
+                    unsigned long long sb = (tgt > 0.f && tid <= dstar) ? bb : 0ull;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) sb = max(sb, __shfl_xor_sync(0xFFFFFFFFu, sb, o));
+                    unsigned long long *wb = reinterpret_cast<unsigned long long *>(sh.hist);
+                    if (lane == 0) wb[warp] = sb;
+                    __syncthreads();
+                    sb = 0ull;
+                    for (int w2 = 0; w2 < kWarps; ++w2) sb = max(sb, wb[w2]);
+                    if (sb != 0ull)
+                        keep_best(key_value(static_cast<uint32_t>(sb >> 32)), static_cast<int32_t>(~static_cast<uint32_t>(sb)),
+                                  best, bi);
+                    y = bi;
+                } else if (ovf || nband > kBandCap) {
                     y = exact_row_token<E>(row, p.V, h, M, info, nz, chunk, sh, ph);
                 } else {
                     const float tgt = rec.target - mass_in;
