@@ -479,103 +479,80 @@ __device__ __forceinline__ float bin_floor_value(int32_t q, float s8)
     return key_value(hi);
 }
 
-// Pass 1 over this thread's 16-byte vectors of the staged chunk: running max
-// with the first index attaining it, and (SUM) sum exp(z - running max)
-// rescaled when the max grows.  The running max starts at a finite sentinel
-// far below any logit, so -inf logits contribute exp(-inf) = 0 without a
-// per-vector test; a chunk of only -inf reports -inf.
+// Pass 1 over this thread's 16-byte vectors of the staged chunk, in two
+// loops.  The first finds the thread's maximum and the first vector holding
+// it with selects only (a running-max update with per-vector rescaling is
+// taken by some lane of the warp on most iterations, so the warp would run
+// it nearly every time); the first index attaining the maximum comes from
+// that vector.  The second loop sums exp(z - max) against the fixed maximum
+// (SUM) and counts z > zd (relaxed mode).  The maximum starts at a finite
+// sentinel far below any logit, so -inf logits contribute exp(-inf) = 0; a
+// chunk of only -inf reports -inf.
 constexpr float kSentinel = -1.0e38f;
-
-// bf16 with the sum: the two halves of each 32-bit word are one f32x2 pair,
-// so the exponent arguments and the two accumulators take packed FMA / ADD
-// (lane 0 sums the even elements, lane 1 the odd ones, in the same order as
-// the scalar form).
-template <int MODE>
-__device__ __forceinline__ float pass1_bf16_sum(const uint4 *body, int nb, int a0, float zd,
-                                                int32_t &targ, float &tsum, int32_t &tcnt)
-{
-    using E = Elt<uint16_t>;
-    float tmax = kSentinel;
-    uint64_t acc = f2_pack(0.f, 0.f);
-    const uint64_t l2 = f2_pack(kLog2e, kLog2e);
-    for (int i = threadIdx.x; i < nb; i += kThreads) {
-        const uint4 v = body[i];
-        const float vm = E::vmax(v);
-        if (vm > tmax) {
-            float x[8];
-            E::unpack(v, x);
-            int first = 7;
-#pragma unroll
-            for (int j = 7; j >= 0; --j)
-                if (x[j] == vm) first = j;
-            const float f = ex2((tmax - vm) * kLog2e);
-            acc = f2_mul(acc, f2_pack(f, f));
-            tmax = vm;
-            targ = a0 + i * 8 + first;
-        }
-        const float c0 = -tmax * kLog2e;
-        const uint64_t c2 = f2_pack(c0, c0);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float e0, e1;
-            f2_unpack(f2_fma(f2_pack(bf_lo(w[j]), bf_hi(w[j])), l2, c2), e0, e1);
-            acc = f2_add(acc, f2_pack(ex2(e0), ex2(e1)));
-        }
-        if (MODE == MODE_RELAXED) {
-            float x[8];
-            E::unpack(v, x);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) tcnt += (x[j] > zd) ? 1 : 0;
-        }
-    }
-    float s0, s1;
-    f2_unpack(acc, s0, s1);
-    tsum = s0 + s1;
-    if (tmax == kSentinel) { tmax = -INFINITY; tsum = 0.f; }
-    return tmax;
-}
 
 template <typename E, int MODE, bool SUM>
 __device__ __forceinline__ float pass1(const uint4 *body, int nb, int a0, float zd, int32_t &targ,
                                        float &tsum, int32_t &tcnt)
 {
-    if constexpr (E::BYTES == 2 && SUM) return pass1_bf16_sum<MODE>(body, nb, a0, zd, targ, tsum, tcnt);
     constexpr int VEC = E::VEC;
     float tmax = kSentinel;
-    float s0 = 0.f, s1 = 0.f;     // two accumulators: independent add chains
-    for (int i = threadIdx.x; i < nb; i += kThreads) {
-        const uint4 v = body[i];
-        const float vm = E::vmax(v);
+    int jmax = -1;
+    for (int i = threadIdx.x, j = 0; i < nb; i += kThreads, ++j) {
+        const float vm = E::vmax(body[i]);
+        jmax = (vm > tmax) ? j : jmax;
+        tmax = fmaxf(tmax, vm);
+    }
+    if (jmax >= 0) {
+        const int i = threadIdx.x + jmax * kThreads;
         float x[VEC];
-        E::unpack(v, x);
-        if (vm > tmax) {
-            int first = VEC - 1;
+        E::unpack(body[i], x);
+        int first = VEC - 1;
 #pragma unroll
-            for (int j = VEC - 1; j >= 0; --j)
-                if (x[j] == vm) first = j;
-            if (SUM) {
-                const float f = ex2((tmax - vm) * kLog2e);
-                s0 *= f;
-                s1 *= f;
+        for (int q = VEC - 1; q >= 0; --q)
+            if (x[q] == tmax) first = q;
+        targ = a0 + i * VEC + first;
+    }
+    if (SUM || MODE == MODE_RELAXED) {
+        const float c0 = -tmax * kLog2e;
+        if constexpr (E::BYTES == 2) {
+            // the two halves of each 32-bit word are one f32x2 pair: packed
+            // exponent arguments and two packed accumulators
+            uint64_t acc = f2_pack(0.f, 0.f);
+            const uint64_t l2 = f2_pack(kLog2e, kLog2e), c2 = f2_pack(c0, c0);
+            for (int i = threadIdx.x; i < nb; i += kThreads) {
+                const uint4 v = body[i];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float lo = bf_lo(w[j]), hi = bf_hi(w[j]);
+                    if (SUM) {
+                        float e0, e1;
+                        f2_unpack(f2_fma(f2_pack(lo, hi), l2, c2), e0, e1);
+                        acc = f2_add(acc, f2_pack(ex2(e0), ex2(e1)));
+                    }
+                    if (MODE == MODE_RELAXED) tcnt += ((lo > zd) ? 1 : 0) + ((hi > zd) ? 1 : 0);
+                }
             }
-            tmax = vm;
-            targ = a0 + i * VEC + first;
-        }
-        if (SUM) {
-            const float c0 = -tmax * kLog2e;
+            float s0, s1;
+            f2_unpack(acc, s0, s1);
+            tsum = s0 + s1;
+        } else {
+            float s0 = 0.f, s1 = 0.f;     // two accumulators: independent add chains
+            for (int i = threadIdx.x; i < nb; i += kThreads) {
+                float x[VEC];
+                E::unpack(body[i], x);
 #pragma unroll
-            for (int j = 0; j < VEC; j += 2) {
-                s0 += ex2(fmaf(x[j], kLog2e, c0));
-                s1 += ex2(fmaf(x[j + 1], kLog2e, c0));
+                for (int j = 0; j < VEC; j += 2) {
+                    if (SUM) {
+                        s0 += ex2(fmaf(x[j], kLog2e, c0));
+                        s1 += ex2(fmaf(x[j + 1], kLog2e, c0));
+                    }
+                    if (MODE == MODE_RELAXED) tcnt += ((x[j] > zd) ? 1 : 0) + ((x[j + 1] > zd) ? 1 : 0);
+                }
             }
-        }
-        if (MODE == MODE_RELAXED) {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) tcnt += (x[j] > zd) ? 1 : 0;
+            tsum = s0 + s1;
         }
     }
-    tsum = s0 + s1;
     if (tmax == kSentinel) { tmax = -INFINITY; tsum = 0.f; }
     return tmax;
 }
