@@ -410,19 +410,29 @@ __device__ __forceinline__ void keep_best(float s, int32_t ix, float &best, int3
     if (s > best || (s == best && ix < bi)) { best = s; bi = ix; }
 }
 
-// scores of the VEC elements of one vector starting at element `base`, a
-// multiple of 4 (the vector covers whole Philox blocks)
+// Scores of the VEC elements of one vector starting at element `base`, a
+// multiple of 4 (the vector covers whole Philox blocks), whose largest value
+// is vm.  An element can only reach `best` if its Gumbel noise -log(-log u)
+// reaches best - z/T, i.e. -log u <= D = exp(z/T - best) <= exp(vm/T - best);
+// as -log u >= 1 - u, an element with 1 - u > D cannot, and for u on the
+// lattice (2k + 1) 2^-24 (k = word >> 9) that is k < (2^24 - 1 - D 2^24) / 2.
+// Those are skipped without the logarithms (one below the bound, for the
+// rounding of D); the others are scored as usual.
 template <int VEC>
-__device__ __forceinline__ void score_vec(const float (&x)[VEC], int32_t base, float invT,
+__device__ __forceinline__ void score_vec(const float (&x)[VEC], float vm, int32_t base, float invT,
                                           const Noise &nz, float &best, int32_t &bi)
 {
+    const float D = ex2((vm * invT - best) * kLog2e);
+    const float t = fmaf(-D, 16777216.f, 16777215.f) * 0.5f;
+    const uint32_t kthr = (t >= 2.f) ? static_cast<uint32_t>(t) - 1u : 0u;
 #pragma unroll
     for (int h = 0; h < VEC / 4; ++h) {
         const uint4 w = nz.block((static_cast<uint32_t>(base) >> 2) + h);
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            keep_best(fmaf(x[4 * h + j], invT, gumbel_of(ws[j])), base + 4 * h + j, best, bi);
+            if ((ws[j] >> 9) >= kthr)
+                keep_best(fmaf(x[4 * h + j], invT, gumbel_of(ws[j])), base + 4 * h + j, best, bi);
     }
 }
 
@@ -885,12 +895,13 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
             const bool whole_blocks = (g.a0 & 3) == 0;
             for (int i = tid; i < g.nb; i += kThreads) {
                 const uint4 v = body[i];
-                if (!(E::vmax(v) >= skip)) continue;
+                const float vm = E::vmax(v);
+                if (!(vm >= skip)) continue;
                 float x[VEC];
                 E::unpack(v, x);
                 const int32_t base = g.a0 + i * VEC;
                 if (whole_blocks) {
-                    score_vec<VEC>(x, base, invT, nz, best, bi);
+                    score_vec<VEC>(x, vm, base, invT, nz, best, bi);
                 } else {
 #pragma unroll
                     for (int q = 0; q < VEC; ++q) keep_best(nz.score(x[q], base + q, invT), base + q, best, bi);
