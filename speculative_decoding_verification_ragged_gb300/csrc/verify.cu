@@ -74,7 +74,9 @@ constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: adding it leaves integer 
 constexpr int32_t kNoBins = INT_MIN;    // chunk grid origin too large for exact bins
 constexpr int kBandCap = 2048;          // undecided values kept on chip
 constexpr int kListCap = 2048;          // candidates the finish kernel stages on chip
-constexpr int kSureCap = 2048;          // heavy kernel: nucleus values compacted per chunk
+constexpr int kPieceBytes = kChunkBytes / 2;   // heavy kernel: half a chunk per work item
+constexpr int kSureH = 1024;            // heavy kernel: values >= zband compacted per piece
+constexpr int kPieceList = kCandCap / 2;        // heavy kernel: band list entries per piece
 constexpr int kFineBand = 64;           // heavy kernel: distinct bf16 band values tallied per chunk
 constexpr int kRowStage = 16 * 1024;    // heavy kernel: bytes per row-streaming stage
 constexpr int kPureListK = 64;          // pure top-p: list above the 64-th thread maximum
@@ -105,7 +107,11 @@ struct __align__(16) ChunkPart {
 };
 static_assert(sizeof(ChunkPart) == 32, "chunk summary is 32 bytes");
 static_assert(kChunkBytes / 16 <= 32 * kThreads, "a thread's vectors of a chunk fit a 32-bit mask");
-static_assert(2 * kRowStage <= kChunkBytes, "the heavy kernel streams rows through its chunk buffer");
+static_assert(2 * kRowStage <= kChunkBytes, "a chunk buffer holds two row stages");
+static_assert(2 * kRowStage <= kPieceBytes + (kSureH + kBandCap) * 8,
+              "the heavy kernel streams rows through its piece, compaction and band space");
+static_assert(kPieceBytes / 16 <= 32 * kThreads, "a thread's vectors of a piece fit a 32-bit mask");
+static_assert(kFineBand * 12 <= kPieceList * 8, "a piece's value tallies fit its list space");
 
 // Record of a row queued for the heavy kernel (32 bytes, at the start of the
 // row's bin area, whose bins are no longer needed).
@@ -134,7 +140,7 @@ struct __align__(16) Shared {
     uint32_t scan[kWarps];
     float red_f[kWarps * 2];
     int32_t red_i[kWarps * 2];
-    int32_t offs[kMaxChunks + 1];
+    int32_t offs[2 * kMaxChunks + 1];
     float M, S, W, sel_excl_f, theta;
     int32_t AMAX, CNT, sel_bin, sel_found, total, overflow, cand_n, R, J, nobins, last, heavy;
     uint32_t sel_excl_u, lkey;
@@ -1590,23 +1596,24 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
 // exact mass select and runs the request chain.  A row queued whole: the CTA
 // of its first chunk runs the exact selects over the row.
 template <typename TIn>
-__global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyParams p)
+__global__ void __launch_bounds__(kThreads, 4) heavy_rows_kernel(const VerifyParams p)
 {
     using E = Elt<TIn>;
     constexpr int VEC = E::VEC;
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *chunk = smem;                                   // one chunk, or two row stages
-    Shared &sh = *reinterpret_cast<Shared *>(smem + kChunkBytes);
-    Cand *sure = reinterpret_cast<Cand *>(reinterpret_cast<uint8_t *>(&sh) + sizeof(Shared));
-    Cand *band = sure + kSureCap;
+    uint8_t *chunk = smem;                                   // one piece; from here 32 KiB of row stages
+    Cand *sure = reinterpret_cast<Cand *>(smem + kPieceBytes);                      // [kSureH]
+    Cand *band = sure + kSureH;                                                     // [kBandCap]
+    Shared &sh = *reinterpret_cast<Shared *>(band + kBandCap);
     __shared__ uint32_t ph[2];
     __shared__ HeavyRec rec_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nchunk = p.nchunk;
+    const int npc = 2 * nchunk;             // pieces per row: the halves of its chunks
 
     griddep_wait();                         // the finish kernel's queue is complete
     const int n_heavy = __ldcg(p.ws_hrows);
-    const int64_t n_items = static_cast<int64_t>(n_heavy) * nchunk;
+    const int64_t n_items = static_cast<int64_t>(n_heavy) * npc;
     if (static_cast<int64_t>(blockIdx.x) >= n_items) return;
     if (tid == 0) {
         mbar_init(&sh.mbar[0], 1);
@@ -1616,19 +1623,27 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
         sh.timeout = 0;
     }
     for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const int hr = static_cast<int>(it / nchunk);
-        const int c = static_cast<int>(it - static_cast<int64_t>(hr) * nchunk);
+        const int hr = static_cast<int>(it / npc);
+        const int pc = static_cast<int>(it - static_cast<int64_t>(hr) * npc);
+        const int c = pc >> 1, half = pc & 1;
         const int r = __ldcg(p.ws_hrows + 1 + hr);
         float *area = p.ws_bins + static_cast<int64_t>(r) * nchunk * kBins;
         const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
-        const ChunkGeom g = chunk_geom<E>(row, c, p.V);
+        ChunkGeom g = chunk_geom<E>(row, c, p.V);
+        // this half of the chunk's body: vectors [pv0, pv0 + g.nb) after the
+        // split; the chunk's unaligned head and tail go with half 0
+        const int nb0 = (g.nb + 1) / 2;
+        const int pv0 = half ? nb0 : 0;
+        g.nb = half ? g.nb - nb0 : nb0;
+        if (half) g.n_extra = 0;
+        const int32_t a0p = g.a0 + pv0 * VEC;
         if (tid == 0) {
-            // the chunk's copy first (in bounds for any queued row), then the
+            // the piece's copy first (in bounds for any queued row), then the
             // row's record and parameters while it is in flight
             const uint32_t bytes = static_cast<uint32_t>(g.nb) * 16u;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&sh.mbar[0], bytes);
-            if (bytes) bulk_g2s(chunk, row + g.a0, bytes, &sh.mbar[0]);
+            if (bytes) bulk_g2s(chunk, row + a0p, bytes, &sh.mbar[0]);
             sh.info = reinterpret_cast<const RowInfo *>(p.ws_info)[r];
             const float4 a = __ldcg(reinterpret_cast<const float4 *>(area));
             const float4 b = __ldcg(reinterpret_cast<const float4 *>(area) + 1);
@@ -1666,7 +1681,7 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
         int32_t y = INT_MAX;
         bool settle = false;
         if (rec.mode == kHeavyWhole) {
-            if (c == 0) {
+            if (pc == 0) {
                 y = exact_row_token<E>(row, p.V, h, M, info, nz, chunk, sh, ph);
                 settle = true;
             }
@@ -1693,7 +1708,7 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                                             static_cast<uint32_t>(~ix));
                 } else {
                     const int slot = warp_append(&sh.total);
-                    if (slot < kCandCap) { band[slot].v = v; band[slot].i = ix; }
+                    if (slot < kPieceList) { band[slot].v = v; band[slot].i = ix; }
                 }
             };
             float mass = 0.f, best = -INFINITY;
@@ -1742,15 +1757,15 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
 #pragma unroll
                 for (int q = 0; q < VEC; ++q)
                     if (x[q] >= zband) {
-                        if (off < kSureCap) { sure[off].v = x[q]; sure[off].i = g.a0 + i * VEC + q; }
+                        if (off < kSureH) { sure[off].v = x[q]; sure[off].i = a0p + i * VEC + q; }
                         ++off;
                     }
             }
             if (xin) {
-                if (off < kSureCap) { sure[off].v = xe; sure[off].i = ie; }
+                if (off < kSureH) { sure[off].v = xe; sure[off].i = ie; }
                 ++off;
             }
-            if (tot > kSureCap) {
+            if (tot > kSureH) {
                 // rare: the values past the buffer are handled where they are
                 auto direct = [&](float v, int32_t ix) {
                     if (v >= zin) {
@@ -1771,16 +1786,16 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                     E::unpack(v, x);
                     for (int q = 0; q < VEC; ++q)
                         if (x[q] >= zband) {
-                            if (o2 >= kSureCap) direct(x[q], g.a0 + i * VEC + q);
+                            if (o2 >= kSureH) direct(x[q], a0p + i * VEC + q);
                             ++o2;
                         }
                 }
-                if (xin && o2 >= kSureCap) direct(xe, ie);
+                if (xin && o2 >= kSureH) direct(xe, ie);
             }
             __syncthreads();
             // the collected values with all lanes busy: nucleus values add
             // their mass and their Gumbel score, band values go to the band
-            const int n_sel = min(tot, kSureCap);
+            const int n_sel = min(tot, kSureH);
             for (int i = tid; i < n_sel; i += kThreads) {
                 const Cand e = sure[i];
                 if (e.v >= zin) {
@@ -1791,10 +1806,10 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                 }
             }
             __syncthreads();
-            // the chunk's band values (or tallies) to its own list space (no
+            // the piece's band values (or tallies) to its own list space (no
             // global atomics)
             const int tb = sh.total;
-            float2 *clist = blist + static_cast<int64_t>(c) * kCandCap;
+            float2 *clist = blist + static_cast<int64_t>(pc) * kPieceList;
             if (fine) {
                 uint32_t *oc = reinterpret_cast<uint32_t *>(clist);
                 if (tid < kFineBand) {
@@ -1802,7 +1817,7 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                     reinterpret_cast<unsigned long long *>(oc + kFineBand)[tid] = fbst[tid];
                 }
             } else {
-                for (int i = tid; i < min(tb, kCandCap); i += kThreads)
+                for (int i = tid; i < min(tb, kPieceList); i += kThreads)
                     clist[i] = make_float2(band[i].v, __int_as_float(band[i].i));
             }
             block_best(best, bi, sh);
@@ -1813,11 +1828,11 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                 hp.bi = bi;
                 hp.mass = mass;
                 hp.nband = tb;
-                reinterpret_cast<HeavyPart *>(area + 8)[c] = hp;
+                reinterpret_cast<HeavyPart *>(area + 8)[pc] = hp;
                 // publish the chunk's results and list, then count
                 fence_acq_rel_gpu();
                 const uint32_t t = atomicAdd(p.ws_rticket + r, 1u);
-                if (t == static_cast<uint32_t>(nchunk - 1)) {
+                if (t == static_cast<uint32_t>(npc - 1)) {
                     fence_acq_rel_gpu();
                     sh.last = 1;
                 }
@@ -1827,22 +1842,22 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                 // ---- the row's last chunk: settle the band ----
                 // the row's chunk results, loaded by one thread each
                 float4 *hps = reinterpret_cast<float4 *>(band);
-                if (tid < nchunk)
+                if (tid < npc)
                     hps[tid] = __ldcg(reinterpret_cast<const float4 *>(reinterpret_cast<const HeavyPart *>(area + 8) + tid));
                 __syncthreads();
                 if (tid == 0) {
                     float bsum = 0.f, bb = -INFINITY;
                     int32_t bbi = INT_MAX, tot = 0, ovf = 0;
-                    for (int q = 0; q < nchunk; ++q) {
+                    for (int q = 0; q < npc; ++q) {
                         const float4 e = hps[q];
                         bsum += e.z;
                         keep_best(e.x, __float_as_int(e.y), bb, bbi);
                         const int nq = __float_as_int(e.w);
                         sh.offs[q] = tot;
-                        ovf |= (nq > kCandCap);
-                        tot += min(nq, kCandCap);
+                        ovf |= (nq > kPieceList);
+                        tot += min(nq, kPieceList);
                     }
-                    sh.offs[nchunk] = tot;
+                    sh.offs[npc] = tot;
                     sh.W = bsum;
                     sh.red_f[0] = bb;
                     sh.red_i[0] = bbi;
@@ -1867,8 +1882,8 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                     uint32_t n = 0;
                     unsigned long long bb = 0ull;
                     if (tid < kFineBand) {
-                        for (int q = 0; q < nchunk; ++q) {
-                            const uint32_t *oc = reinterpret_cast<const uint32_t *>(blist + static_cast<int64_t>(q) * kCandCap);
+                        for (int q = 0; q < npc; ++q) {
+                            const uint32_t *oc = reinterpret_cast<const uint32_t *>(blist + static_cast<int64_t>(q) * kPieceList);
                             n += __ldcg(oc + tid);
                             bb = max(bb, __ldcg(reinterpret_cast<const unsigned long long *>(oc + kFineBand) + tid));
                         }
@@ -1910,7 +1925,7 @@ __global__ void __launch_bounds__(kThreads, 3) heavy_rows_kernel(const VerifyPar
                         for (int e = tid; e < nband; e += kThreads) {
                             int q = 0;
                             while (sh.offs[q + 1] <= e) ++q;
-                            const float2 v = __ldcg(blist + static_cast<int64_t>(q) * kCandCap + (e - sh.offs[q]));
+                            const float2 v = __ldcg(blist + static_cast<int64_t>(q) * kPieceList + (e - sh.offs[q]));
                             band[e].v = v.x;
                             band[e].i = __float_as_int(v.y);
                         }
@@ -1969,8 +1984,8 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
         smem += static_cast<size_t>(kCandCap) * sizeof(Cand) + static_cast<size_t>(kWarps) * kBins * 4;
     const size_t smem_fin = sizeof(Shared) + kMaxChunks * sizeof(ChunkPart) +
                             static_cast<size_t>(kBandCap + kListCap) * sizeof(Cand);
-    const size_t smem_heavy = kChunkBytes + sizeof(Shared) +
-                              static_cast<size_t>(kSureCap + kBandCap) * sizeof(Cand);
+    const size_t smem_heavy = kPieceBytes + sizeof(Shared) +
+                              static_cast<size_t>(kSureH + kBandCap) * sizeof(Cand);
     auto kstream = stream_chunks_kernel<TIn, MODE>;
     auto kfin = finish_rows_kernel<TIn, MODE>;
     auto kheavy = heavy_rows_kernel<TIn>;
@@ -2041,7 +2056,7 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     if (e != cudaSuccess || MODE != MODE_SAMPLE) return e;
     // heavy rows: persistent over whatever the finish kernel queued
     cudaLaunchConfig_t ch = {};
-    ch.gridDim = dim3(static_cast<unsigned>(3 * nsm), 1, 1);
+    ch.gridDim = dim3(static_cast<unsigned>(4 * nsm), 1, 1);
     ch.blockDim = dim3(kThreads, 1, 1);
     ch.dynamicSmemBytes = smem_heavy;
     ch.stream = stream;
