@@ -78,6 +78,7 @@ constexpr int kPieceBytes = kChunkBytes / 2;   // heavy kernel: half a chunk per
 constexpr int kSureH = 1024;            // heavy kernel: values >= zband compacted per piece
 constexpr int kPieceList = kCandCap / 2;        // heavy kernel: band list entries per piece
 constexpr int kFineBand = 64;           // heavy kernel: distinct bf16 band values tallied per chunk
+constexpr int kTally = 128;             // finish kernel: bf16 values a top-p tally covers
 constexpr int kRowStage = 16 * 1024;    // heavy kernel: bytes per row-streaming stage
 constexpr int kPureListK = 64;          // pure top-p: list above the 64-th thread maximum
 constexpr float kMassTol = 1e-5f;       // relative slack of the bin bracket
@@ -1238,6 +1239,81 @@ __device__ __forceinline__ void request_chain(const VerifyParams &p, const RowIn
     }
 }
 
+// The key of the smallest bf16 value whose order-preserving key is >= k.
+__device__ __forceinline__ uint32_t bf16_key_ceil(uint32_t k)
+{
+    const uint32_t h = k >> 16;
+    const uint32_t full = (h << 16) | ((h & 0x8000u) ? 0u : 0xFFFFu);
+    return (full >= k) ? h : h + 1u;
+}
+
+// Top-p over a set of bf16 values tallied per value (d = ktop - key, below
+// kTally): a count and the best Gumbel score packed with its index.  Equal
+// values share their weight exp((z - M)/T), so the running mass from the
+// top value is exact per value group.  `visit` yields every value of the set
+// (all values with key in [klo, ktop]); the target is frac times their total
+// mass (frac > 0) or target_abs, which the total must exceed by kMassTol
+// relative (else false: the set does not hold the boundary).  On success the
+// best score among the values down to the boundary value is in best / bi.
+template <typename Visit>
+__device__ bool tally_top_p(Visit &&visit, uint32_t klo, uint32_t ktop, float M, float sc,
+                            GumbelScorer &gs, float frac, float target_abs, uint32_t *cnt,
+                            unsigned long long *bst, float &best, int32_t &bi, Shared &sh)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < kTally) { cnt[tid] = 0u; bst[tid] = 0ull; }
+    __syncthreads();
+    visit([&](float v, int32_t ix) {
+        const uint32_t d = ktop - (fkey(v) >> 16);
+        atomicAdd(cnt + d, 1u);
+        atomicMax(bst + d, (static_cast<unsigned long long>(fkey(gs(v, ix))) << 32) |
+                               static_cast<uint32_t>(~ix));
+    }, key_floor((klo << 16) | ((klo & 0x8000u) ? 0u : 0xFFFFu)));
+    __syncthreads();
+    float w = 0.f;
+    if (tid < kTally && cnt[tid]) {
+        const uint32_t k = ktop - static_cast<uint32_t>(tid);
+        w = static_cast<float>(cnt[tid]) * ex2((key_value((k << 16) | ((k & 0x8000u) ? 0u : 0xFFFFu)) - M) * sc);
+    }
+    float cum = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xFFFFFFFFu, cum, o);
+        if (lane >= o) cum += u;
+    }
+    float *wt = reinterpret_cast<float *>(sh.scan);
+    if (lane == 31) wt[warp] = cum;
+    __syncthreads();
+    float total = 0.f;
+    for (int w2 = 0; w2 < kTally / 32; ++w2) {
+        if (w2 < warp) cum += wt[w2];
+        total += wt[w2];
+    }
+    const float target = (frac > 0.f) ? frac * total : target_abs;
+    const bool ok = (frac > 0.f) || total >= target_abs * (1.f + kMassTol);
+    if (!ok) {
+        __syncthreads();
+        return false;
+    }
+    const int dstar = min(__syncthreads_count(tid < kTally && cum < target), kTally - 1);
+    unsigned long long sb = (tid < kTally && tid <= dstar) ? bst[tid] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sb = max(sb, __shfl_xor_sync(0xFFFFFFFFu, sb, o));
+    unsigned long long *wb = reinterpret_cast<unsigned long long *>(sh.hist);
+    if (lane == 0) wb[warp] = sb;
+    __syncthreads();
+    sb = 0ull;
+    for (int w2 = 0; w2 < kWarps; ++w2) sb = max(sb, wb[w2]);
+    best = -INFINITY;
+    bi = INT_MAX;
+    if (sb != 0ull) {
+        best = key_value(static_cast<uint32_t>(sb >> 32));
+        bi = static_cast<int32_t>(~static_cast<uint32_t>(sb));
+    }
+    __syncthreads();
+    return true;
+}
+
 // ------------------------------------------------------ finish kernel ----
 
 // One CTA per packed row, after the stream kernel: combine the chunk
@@ -1415,9 +1491,23 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
                 __syncthreads();
                 const float target = info.top_p * sh.W;
                 const int32_t J = sh.J;
-                heavy = sh.nobins ? kHeavyWhole : 0;
+                bool settled = false, listed = false;
+                if (E::BYTES == 2 && staged) {
+                    // every value at or above the highest list level is
+                    // listed: when they span at most kTally bf16 values and
+                    // hold the target mass, their tally settles the row
+                    const uint32_t klo = bf16_key_ceil(fkey(sh.theta)), ktop = keyM >> 16;
+                    if (ktop >= klo && ktop - klo < static_cast<uint32_t>(kTally)) {
+                        stage_lists();
+                        listed = true;
+                        uint32_t *cnt = reinterpret_cast<uint32_t *>(band);
+                        settled = tally_top_p(visit_lst, klo, ktop, M, sc, gs, 0.f, target, cnt,
+                                              reinterpret_cast<unsigned long long *>(cnt + kTally), best, bi, sh);
+                    }
+                }
+                heavy = (!settled && sh.nobins) ? kHeavyWhole : 0;
                 int32_t qin = 0, qband = 0;
-                if (!heavy) {
+                if (!settled && !heavy) {
                     // combined mass of absolute bin J - t, then C(t) = mass of
                     // bins J - t .. J (thread t)
                     // the row's bins staged in shared memory by all threads
@@ -1460,9 +1550,9 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
                 }
                 // the lists cover the band when every value below the highest
                 // list level falls in a bin below the band
-                if (!heavy && !(staged && abs_bin(sh.theta, s8) < qband)) heavy = kHeavyBand;
-                if (!heavy) {
-                    stage_lists();
+                if (!settled && !heavy && !(staged && abs_bin(sh.theta, s8) < qband)) heavy = kHeavyBand;
+                if (!settled && !heavy) {
+                    if (!listed) stage_lists();
                     if (tid == 0) sh.cand_n = 0;
                     __syncthreads();
                     float mass_in = 0.f;
@@ -1497,7 +1587,7 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
                         }, -INFINITY);
                     }
                     block_best(best, bi, sh);
-                } else if (tid == 0) {
+                } else if (heavy && tid == 0) {
                     hrec.mode = heavy;
                     hrec.amax = AMAX;
                     hrec.qin = qin;
@@ -1528,22 +1618,36 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
                     key_S = max(key_S, select_key<E, false>(visit, lo_k, keyM, 0.f,
                                                             static_cast<uint32_t>(info.top_k), M,
                                                             sc, sh));
-                uint32_t key_F = key_S;
-                if (f.use_p) {
-                    float w = 0.f;
-                    const uint32_t kS = key_S;
-                    visit([&](float v, int32_t) {
-                        if (fkey(v) >= kS) w += ex2((v - M) * sc);
-                    }, key_floor(key_S));
-                    const float Wt = block_sum(w, sh);
-                    key_F = max(key_S, select_key<E, true>(visit, key_S, keyM, info.top_p * Wt, 0u,
-                                                           M, sc, sh));
+                bool tallied = false;
+                if (E::BYTES == 2 && f.use_p) {
+                    // the survivors tallied per value when they span at most
+                    // kTally bf16 values
+                    const uint32_t klo = bf16_key_ceil(key_S), ktop = keyM >> 16;
+                    if (ktop >= klo && ktop - klo < static_cast<uint32_t>(kTally)) {
+                        uint32_t *cnt = reinterpret_cast<uint32_t *>(band);
+                        tally_top_p(visit, klo, ktop, M, sc, gs, info.top_p, 0.f, cnt,
+                                    reinterpret_cast<unsigned long long *>(cnt + kTally), best, bi, sh);
+                        tallied = true;
+                    }
                 }
-                const uint32_t kF = key_F;
-                visit([&](float v, int32_t ix) {
-                    if (fkey(v) >= kF) score_all(v, ix);
-                }, key_floor(key_F));
-                block_best(best, bi, sh);
+                if (!tallied) {
+                    uint32_t key_F = key_S;
+                    if (f.use_p) {
+                        float w = 0.f;
+                        const uint32_t kS = key_S;
+                        visit([&](float v, int32_t) {
+                            if (fkey(v) >= kS) w += ex2((v - M) * sc);
+                        }, key_floor(key_S));
+                        const float Wt = block_sum(w, sh);
+                        key_F = max(key_S, select_key<E, true>(visit, key_S, keyM, info.top_p * Wt, 0u,
+                                                               M, sc, sh));
+                    }
+                    const uint32_t kF = key_F;
+                    visit([&](float v, int32_t ix) {
+                        if (fkey(v) >= kF) score_all(v, ix);
+                    }, key_floor(key_F));
+                    block_best(best, bi, sh);
+                }
             }
         }
         if (heavy && tid == 0) {
