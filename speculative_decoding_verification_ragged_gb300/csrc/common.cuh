@@ -199,15 +199,18 @@ __device__ __forceinline__ float key_value(uint32_t k)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// max of the 8 bf16 values of a 16-byte vector, as float (packed compares)
+// max of the 8 bf16 values of a 16-byte vector, as float: packed bf16x2
+// maxima on the 32-bit words themselves (no detour through memory)
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t m;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+    return m;
+}
+
 __device__ __forceinline__ float vmax_bf16(uint4 v)
 {
-    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&v.x);
-    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&v.y);
-    __nv_bfloat162 c = *reinterpret_cast<__nv_bfloat162 *>(&v.z);
-    __nv_bfloat162 d = *reinterpret_cast<__nv_bfloat162 *>(&v.w);
-    __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
-    uint32_t w = *reinterpret_cast<uint32_t *>(&m);
+    const uint32_t w = max_bf16x2(max_bf16x2(v.x, v.y), max_bf16x2(v.z, v.w));
     return fmaxf(bf_lo(w), bf_hi(w));
 }
 
