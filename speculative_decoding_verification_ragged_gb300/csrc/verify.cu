@@ -790,15 +790,20 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nchunk = p.nchunk;
-    // The sampler takes chunk-major order (CTA b: chunk b / rows of row
-    // b % rows): a chunk's cost depends on its row's filters, and this
-    // spreads every row's chunks evenly over the grid, with the short tail
-    // chunks in the last wave.  Uniform modes keep row-major order.
+    // The sampler takes chunk-major order: a chunk's cost depends on its
+    // row's filters, and this spreads every row's chunks evenly over the
+    // grid, with the short tail chunks in the last wave.  Uniform modes keep
+    // row-major order.  The grid is two-dimensional with the faster index in
+    // x (sampler: x = row, y = chunk; else x = chunk, y = row), so the order
+    // comes without divisions; row-major grids of more than 65535 rows are
+    // one-dimensional.
     int r, c;
     if (MODE == MODE_SAMPLE) {
-        const int rows = static_cast<int>(gridDim.x) / nchunk;
-        c = static_cast<int>(blockIdx.x) / rows;
-        r = static_cast<int>(blockIdx.x) - c * rows;
+        r = static_cast<int>(blockIdx.x);
+        c = static_cast<int>(blockIdx.y);
+    } else if (gridDim.y > 1 || gridDim.x == static_cast<unsigned>(nchunk)) {
+        c = static_cast<int>(blockIdx.x);
+        r = static_cast<int>(blockIdx.y);
     } else {
         r = static_cast<int>(blockIdx.x) / nchunk;
         c = static_cast<int>(blockIdx.x) - r * nchunk;
@@ -2141,7 +2146,12 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     // one CTA per (row, chunk); the entry points bound rows * nchunk by 2^31 - 1
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(rows) * p.nchunk), 1, 1);
+    if (MODE == MODE_SAMPLE)
+        cfg.gridDim = dim3(static_cast<unsigned>(rows), static_cast<unsigned>(p.nchunk), 1);
+    else if (rows <= 65535)
+        cfg.gridDim = dim3(static_cast<unsigned>(p.nchunk), static_cast<unsigned>(rows), 1);
+    else
+        cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(rows) * p.nchunk), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
