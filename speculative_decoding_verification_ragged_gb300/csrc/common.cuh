@@ -121,6 +121,14 @@ __device__ __forceinline__ void fence_acq_rel_gpu()
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
+// Maximum of a float over the full warp (NaN operands ignored, as fmaxf).
+__device__ __forceinline__ float warp_max_f32(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float ex2(float x)
 {
     float y;

@@ -723,12 +723,9 @@ __device__ __forceinline__ void chunk_reduce(float tmax, int32_t targ, float tsu
                                              bool need_sum, Shared &sh)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float wm = tmax;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
-    int32_t wa = (tmax == wm) ? targ : INT_MAX;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wa = min(wa, __shfl_xor_sync(0xFFFFFFFFu, wa, o));
+    // warp maximum, then the lowest index attaining it (indices are >= 0)
+    const float wm = warp_max_f32(tmax);
+    const int32_t wa = __reduce_min_sync(0xFFFFFFFFu, (tmax == wm) ? targ : INT_MAX);
     float ws = 0.f;
     if (need_sum) {
         ws = (tmax > -INFINITY) ? tsum * ex2((tmax - wm) * kLog2e) : 0.f;
@@ -736,11 +733,7 @@ __device__ __forceinline__ void chunk_reduce(float tmax, int32_t targ, float tsu
         for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, o);
     }
     int32_t wc = 0;
-    if (MODE == MODE_RELAXED) {
-        wc = tcnt;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) wc += __shfl_xor_sync(0xFFFFFFFFu, wc, o);
-    }
+    if (MODE == MODE_RELAXED) wc = __reduce_add_sync(0xFFFFFFFFu, tcnt);
     if (lane == 0) {
         sh.red_f[warp] = wm; sh.red_f[kWarps + warp] = ws;
         sh.red_i[warp] = wa; sh.red_i[kWarps + warp] = wc;
@@ -749,21 +742,15 @@ __device__ __forceinline__ void chunk_reduce(float tmax, int32_t targ, float tsu
     if (warp == 0) {
         const bool on = lane < kWarps;
         const float m0 = on ? sh.red_f[lane] : -INFINITY;
-        float m = m0;
-#pragma unroll
-        for (int o = kWarps / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        int32_t a = (on && m0 == m) ? sh.red_i[lane] : INT_MAX;
-#pragma unroll
-        for (int o = kWarps / 2; o > 0; o >>= 1) a = min(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+        const float m = warp_max_f32(m0);
+        const int32_t a = __reduce_min_sync(0xFFFFFFFFu, (on && m0 == m) ? sh.red_i[lane] : INT_MAX);
         float sm_ = 0.f;
         if (need_sum) {
             sm_ = (on && m0 > -INFINITY) ? sh.red_f[kWarps + lane] * ex2((m0 - m) * kLog2e) : 0.f;
 #pragma unroll
             for (int o = kWarps / 2; o > 0; o >>= 1) sm_ += __shfl_xor_sync(0xFFFFFFFFu, sm_, o);
         }
-        int32_t cc = on ? sh.red_i[kWarps + lane] : 0;
-#pragma unroll
-        for (int o = kWarps / 2; o > 0; o >>= 1) cc += __shfl_xor_sync(0xFFFFFFFFu, cc, o);
+        const int32_t cc = __reduce_add_sync(0xFFFFFFFFu, on ? sh.red_i[kWarps + lane] : 0);
         if (lane == 0) {
             sh.part.m = m; sh.part.amax = a; sh.part.s = sm_; sh.part.cnt = cc;
             sh.part.gbest = -INFINITY; sh.part.gidx = INT_MAX; sh.part.ncand = 0;
