@@ -322,12 +322,10 @@ __device__ __forceinline__ float block_sum(float v, Shared &sh)
 // block reduction of a (score, index) maximum, lowest index on ties
 __device__ __forceinline__ void block_best(float &best, int32_t &bi, Shared &sh)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        const int32_t oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-        if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
-    }
+    // the warp's best score, then the lowest index attaining it
+    const float wb = warp_max_f32(best);
+    bi = static_cast<int32_t>(__reduce_min_sync(0xFFFFFFFFu, (best == wb) ? static_cast<uint32_t>(bi) : 0xFFFFFFFFu));
+    best = wb;
     if ((threadIdx.x & 31) == 0) { sh.red_f[threadIdx.x >> 5] = best; sh.red_i[threadIdx.x >> 5] = bi; }
     __syncthreads();
     best = -INFINITY;
@@ -514,6 +512,7 @@ __device__ __forceinline__ float pass1(const uint4 *body, int nb, int a0, float 
     constexpr int VEC = E::VEC;
     float tmax = kSentinel;
     int jmax = -1;
+#pragma unroll 4
     for (int i = threadIdx.x, j = 0; i < nb; i += kThreads, ++j) {
         const float vm = E::vmax(body[i]);
         jmax = (vm > tmax) ? j : jmax;
@@ -536,6 +535,7 @@ __device__ __forceinline__ float pass1(const uint4 *body, int nb, int a0, float 
             // exponent arguments and two packed accumulators
             uint64_t acc = f2_pack(0.f, 0.f);
             const uint64_t l2 = f2_pack(kLog2e, kLog2e), c2 = f2_pack(c0, c0);
+#pragma unroll 4
             for (int i = threadIdx.x; i < nb; i += kThreads) {
                 const uint4 v = body[i];
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
