@@ -129,6 +129,14 @@ __device__ __forceinline__ float warp_max_f32(float v)
     return r;
 }
 
+// Minimum of a float over the full warp (NaN operands ignored, as fminf).
+__device__ __forceinline__ float warp_min_f32(float v)
+{
+    float r;
+    asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float ex2(float x)
 {
     float y;

@@ -1353,23 +1353,26 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
     const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
     const bool need_sum = (MODE == MODE_CONF) || (p.row_lse != nullptr);
 
-    // combine the chunk summaries (warp 0; chunk order fixed)
+    // combine the chunk summaries (warp 0): per lane its chunks, then the
+    // warp's maximum, the lowest index attaining it, the rescaled sums and
+    // the counts
     if (warp == 0) {
         float m = -INFINITY, s = 0.f;
         int32_t a = INT_MAX, cc = 0;
         for (int q = lane; q < nchunk; q += 32)
             combine(m, a, s, cc, parts[q].m, parts[q].amax, parts[q].s, parts[q].cnt, need_sum);
+        const float mw = warp_max_f32(m);
+        const int32_t aw = __reduce_min_sync(0xFFFFFFFFu, (m == mw) ? a : INT_MAX);
+        float sw = 0.f;
+        if (need_sum) {
+            sw = (m > -INFINITY) ? s * ex2((m - mw) * kLog2e) : 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float om = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-            const int32_t oa = __shfl_xor_sync(0xFFFFFFFFu, a, o);
-            const float os = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-            const int32_t oc = __shfl_xor_sync(0xFFFFFFFFu, cc, o);
-            combine(m, a, s, cc, om, oa, os, oc, need_sum);
+            for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xFFFFFFFFu, sw, o);
         }
+        const int32_t cw = __reduce_add_sync(0xFFFFFFFFu, cc);
         if (lane == 0) {
-            sh.M = m; sh.S = s; sh.CNT = cc;
-            sh.AMAX = (m == -INFINITY) ? 0 : a;
+            sh.M = mw; sh.S = sw; sh.CNT = cw;
+            sh.AMAX = (mw == -INFINITY) ? 0 : aw;
         }
     }
     __syncthreads();
@@ -1396,25 +1399,35 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
             for (int q = tid; q < nchunk; q += kThreads) keep_best(parts[q].gbest, parts[q].gidx, best, bi);
             block_best(best, bi, sh);
         } else {
-            // candidate lists: offsets, overflow, the lowest and highest
-            // levels they lie above
-            if (tid == 0) {
+            // candidate lists: offsets (a warp scan), overflow, the lowest
+            // and highest levels they lie above
+            if (warp == 0) {
                 int tot = 0, ovf = 0;
                 float th = -INFINITY, lmin = INFINITY;
-                for (int q = 0; q < nchunk; ++q) {
-                    sh.offs[q] = tot;
-                    if (!(parts[q].m > -INFINITY)) continue;
-                    const int nq = parts[q].ncand;
-                    ovf |= (nq > kCandCap);
-                    tot += min(nq, kCandCap);
-                    th = fmaxf(th, parts[q].lev);
-                    lmin = fminf(lmin, parts[q].lev);
+                for (int q0 = 0; q0 < nchunk; q0 += 32) {
+                    const int q = q0 + lane;
+                    const bool on = q < nchunk && parts[q].m > -INFINITY;
+                    const int nq = on ? parts[q].ncand : 0;
+                    const int nc = min(nq, kCandCap);
+                    int incl = nc;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    if (q < nchunk) sh.offs[q] = tot + incl - nc;
+                    tot += __shfl_sync(0xFFFFFFFFu, incl, 31);
+                    ovf |= static_cast<int>(__reduce_or_sync(0xFFFFFFFFu, (on && nq > kCandCap) ? 1u : 0u));
+                    th = fmaxf(th, warp_max_f32(on ? parts[q].lev : -INFINITY));
+                    lmin = fminf(lmin, warp_min_f32(on ? parts[q].lev : INFINITY));
                 }
-                sh.offs[nchunk] = tot;
-                sh.total = tot;
-                sh.overflow = ovf;
-                sh.theta = th;
-                sh.lkey = (lmin == INFINITY) ? 0u : fkey(lmin);
+                if (lane == 0) {
+                    sh.offs[nchunk] = tot;
+                    sh.total = tot;
+                    sh.overflow = ovf;
+                    sh.theta = th;
+                    sh.lkey = (lmin == INFINITY) ? 0u : fkey(lmin);
+                }
             }
             __syncthreads();
             const int n_list = sh.total;
@@ -1467,18 +1480,25 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
             if (f.pure_p) {
                 // ---- top-p alone: bracket the boundary with the bins ----
                 const float s8 = bin_scale(T);
-                if (tid == 0) {
+                if (warp == 0) {
+                    // the row's mass, the highest grid origin, chunks without bins
                     float w = 0.f;
                     int32_t J = INT_MIN, nob = 0;
-                    for (int q = 0; q < nchunk; ++q) {
-                        if (!(parts[q].m > -INFINITY)) continue;
-                        w += parts[q].gbest * ex2((parts[q].m - M) * sc);
-                        nob |= (parts[q].gidx == kNoBins);
-                        J = max(J, parts[q].gidx);
+                    for (int q0 = 0; q0 < nchunk; q0 += 32) {
+                        const int q = q0 + lane;
+                        const bool on = q < nchunk && parts[q].m > -INFINITY;
+                        float wq = on ? parts[q].gbest * ex2((parts[q].m - M) * sc) : 0.f;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) wq += __shfl_xor_sync(0xFFFFFFFFu, wq, o);
+                        w += wq;
+                        nob |= static_cast<int>(__reduce_or_sync(0xFFFFFFFFu, (on && parts[q].gidx == kNoBins) ? 1u : 0u));
+                        J = max(J, __reduce_max_sync(0xFFFFFFFFu, on ? parts[q].gidx : INT_MIN));
                     }
-                    sh.W = w;
-                    sh.J = J;
-                    sh.nobins = nob;
+                    if (lane == 0) {
+                        sh.W = w;
+                        sh.J = J;
+                        sh.nobins = nob;
+                    }
                 }
                 __syncthreads();
                 const float target = info.top_p * sh.W;
