@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import ctypes
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -46,11 +47,19 @@ KERNEL_SOURCES = ["speculative_decoding_verification_ragged_gb300/csrc/verify.cu
 LAUNCHES_PER_CALL = 4
 
 
+def _code_only(text: str) -> str:
+    """The source without // and /* */ comments or blank lines (comment edits
+    do not change a kernel, so they do not invalidate its counters)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines()]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_digest() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -8,19 +8,22 @@
 //     cu_rows), the row's position and validity and the owner's parameters,
 //     as a 64-byte row record; requests without a valid row range get their
 //     outputs here.
-//   stream, one CTA per (row, chunk of kChunkBytes): thread 0 issues one 1-D
-//     TMA bulk copy of the chunk's 16-byte-aligned body into shared memory
-//     first, then one of the row record on the same mbarrier once the
-//     prologue has finished (the row is read from HBM exactly once;
+//   stream, one CTA per (row, chunk of kChunkBytes) on a two-dimensional
+//     grid (the sampler chunk-major, the other modes row-major): thread 0
+//     issues one 1-D TMA bulk copy of the chunk's 16-byte-aligned body into
+//     shared memory first, then one of the row record on the same mbarrier
+//     once the prologue has finished (the row is read from HBM exactly once;
 //     unaligned head/tail elements use plain loads); many short CTAs per SM
-//     keep the copies in flight.  Pass 1 runs a per-thread online max /
-//     first argmax / sum exp(z - max) over 16-byte vectors (packed f32x2
-//     arithmetic for bf16), plus the count of logits above the draft's logit
-//     for relaxed top-K; warp shuffles and a CTA reduction give the chunk
+//     keep the copies in flight.  Pass 1 takes two loops over the thread's
+//     16-byte vectors: the maximum and the first vector holding it (selects
+//     only), then sum exp(z - max) against it (packed f32x2 arithmetic for
+//     bf16) and the count of logits above the draft's logit for relaxed
+//     top-K; warp reductions (redux.sync) and a CTA reduction give the chunk
 //     summary.  For the sampler (T > 0):
 //       no filter   - the chunk's own Gumbel-max winner (vectors that cannot
 //                     beat a lower bound taken from the thread maxima are
-//                     skipped);
+//                     skipped, and so are the logarithms of elements whose
+//                     uniform cannot reach the running best);
 //       top-k/min-p - the survivors form an upper set {z >= th}; the chunk
 //                     bounds th from below (exact k-th largest of the thread
 //                     maxima; chunk max + T ln min_p) and stores the elements
@@ -35,20 +38,23 @@
 //   finish, one CTA per row: combine the chunk summaries, then for the
 //     sampler run radix selects (exact k-th largest value, exact top-p mass
 //     crossing) over the candidate lists staged in shared memory and
-//     Gumbel-max over the survivors with Philox4x32-10 uniforms.  Pure top-p
-//     brackets the nucleus boundary with the combined bins; when the lists
-//     cover the undecided band the row is settled from them.  A row that
-//     needs its logits again (a nucleus wider than the lists, or a list or
-//     band overflow) is queued for the heavy kernel with a short record.
-//     The CTA finishing the last row of a request (atomic ticket) runs the
-//     accept-while-equal prefix scan with one warp ballot and writes the
-//     request's tokens and the optional prefix-acceptance counters.
-//   heavy (sampler only), persistent over the queued rows' chunks: each
-//     chunk is staged by TMA, its nucleus and band values are compacted in
-//     shared memory and the nucleus scored with all lanes busy, its band
-//     values go to a per-chunk list; the CTA finishing a row's last chunk
-//     (atomic ticket) settles the band exactly, or runs exact selects over
-//     the whole row when a band or list overflowed, then runs the chain.
+//     Gumbel-max over the survivors with Philox4x32-10 uniforms; bf16
+//     survivors spanning at most kTally values take top-p over per-value
+//     tallies instead.  Pure top-p brackets the nucleus boundary with the
+//     combined bins; when the lists cover the undecided band the row is
+//     settled from them.  A row that needs its logits again (a nucleus wider
+//     than the lists, or a list or band overflow) is queued for the heavy
+//     kernel with a short record.  The CTA finishing the last row of a
+//     request (atomic ticket) runs the accept-while-equal prefix scan with
+//     one warp ballot and writes the request's tokens and the optional
+//     prefix-acceptance counters.
+//   heavy (sampler only), persistent over the queued rows' half-chunks:
+//     each piece is staged by TMA, its nucleus and band values are compacted
+//     in shared memory and the nucleus scored with all lanes busy; its band
+//     values go to a per-piece list, or, for a narrow bf16 band, to
+//     per-value tallies.  The CTA finishing a row's last piece (atomic
+//     ticket) settles the band exactly, or runs exact selects over the whole
+//     row when a band or list overflowed, then runs the chain.
 //
 // Definitions: xLLM docs "自适应投机推理" §"启动示例" (ragged rejection
 // sampler with packed-row owners, point-mass draft, replacement / bonus,
@@ -125,12 +131,12 @@ struct __align__(16) HeavyRec {
 };
 static_assert(sizeof(HeavyRec) == 32, "heavy record is 32 bytes");
 
-// per-chunk result of the heavy pass (16 bytes, after the record)
+// per-piece result of the heavy pass (16 bytes each, after the record)
 struct __align__(16) HeavyPart {
-    float best;     // best Gumbel score among the chunk's nucleus values
+    float best;     // best Gumbel score among the piece's nucleus values
     int32_t bi;     //   and its index
     float mass;     // their mass exp((z - M)/T)
-    int32_t nband;  // band values stored in the chunk's list (> kCandCap: overflow)
+    int32_t nband;  // band values stored in the piece's list (> kPieceList: overflow)
 };
 
 // shared scratch common to the row kernels
@@ -1702,15 +1708,17 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
 
 // ------------------------------------------------------- heavy kernel ----
 
-// Persistent over the chunks of the rows the finish kernel queued.  A row
-// queued for its band: every chunk is staged by TMA; its values at or above
-// the band's upper edge are in the nucleus, the values in the band are
-// collected; both are compacted in shared memory (counts, a CTA scan, a
-// scatter: no per-element branches that diverge) and the nucleus is scored
-// with all lanes busy; each chunk's band values go to its own list.  The CTA
-// finishing the row's last chunk (atomic ticket) settles the band with an
-// exact mass select and runs the request chain.  A row queued whole: the CTA
-// of its first chunk runs the exact selects over the row.
+// Persistent over the pieces (half-chunks) of the rows the finish kernel
+// queued.  A row queued for its band: every piece is staged by TMA; its
+// values at or above the band's upper edge are in the nucleus, the values in
+// the band are collected; both are compacted in shared memory (counts, a CTA
+// scan, a scatter: no per-element branches that diverge) and the nucleus is
+// scored with all lanes busy; each piece's band values go to its own list,
+// or to per-value tallies when a bf16 band spans at most kFineBand values.
+// The CTA finishing the row's last piece (atomic ticket) settles the band
+// (a scan of the tallies, or an exact mass select over the lists) and runs
+// the request chain.  A row queued whole: the CTA of its first piece runs
+// the exact selects over the row.
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads, 4) heavy_rows_kernel(const VerifyParams p)
 {
@@ -1802,7 +1810,7 @@ __global__ void __launch_bounds__(kThreads, 4) heavy_rows_kernel(const VerifyPar
                 settle = true;
             }
         } else {
-            // ---- one chunk of a band row ----
+            // ---- one piece of a band row ----
             const float sc = f.sc;
             const float zin = rec.zin, zband = rec.zband;
             float2 *blist = reinterpret_cast<float2 *>(p.ws_cand) +
@@ -1945,7 +1953,7 @@ __global__ void __launch_bounds__(kThreads, 4) heavy_rows_kernel(const VerifyPar
                 hp.mass = mass;
                 hp.nband = tb;
                 reinterpret_cast<HeavyPart *>(area + 8)[pc] = hp;
-                // publish the chunk's results and list, then count
+                // publish the piece's results and list, then count
                 fence_acq_rel_gpu();
                 const uint32_t t = atomicAdd(p.ws_rticket + r, 1u);
                 if (t == static_cast<uint32_t>(npc - 1)) {
@@ -1955,8 +1963,8 @@ __global__ void __launch_bounds__(kThreads, 4) heavy_rows_kernel(const VerifyPar
             }
             __syncthreads();
             if (sh.last) {
-                // ---- the row's last chunk: settle the band ----
-                // the row's chunk results, loaded by one thread each
+                // ---- the row's last piece: settle the band ----
+                // the row's piece results, loaded by one thread each
                 float4 *hps = reinterpret_cast<float4 *>(band);
                 if (tid < npc)
                     hps[tid] = __ldcg(reinterpret_cast<const float4 *>(reinterpret_cast<const HeavyPart *>(area + 8) + tid));
@@ -1989,7 +1997,7 @@ __global__ void __launch_bounds__(kThreads, 4) heavy_rows_kernel(const VerifyPar
                 const bool ovf = sh.overflow != 0;
                 __syncthreads();
                 if (fine) {
-                    // per value: the chunks' counts and best scores; the
+                    // per value: the pieces' counts and best scores; the
                     // running band mass from the top value first reaches
                     // the target at the boundary value (all values when
                     // rounding keeps it short); the best score among the
@@ -2175,7 +2183,7 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     cf.numAttrs = 1;
     e = cudaLaunchKernelEx(&cf, kfin, p);
     if (e != cudaSuccess || MODE != MODE_SAMPLE) return e;
-    // heavy rows: persistent over whatever the finish kernel queued
+    // heavy rows: persistent over the pieces of whatever the finish kernel queued
     cudaLaunchConfig_t ch = {};
     ch.gridDim = dim3(static_cast<unsigned>(4 * nsm), 1, 1);
     ch.blockDim = dim3(kThreads, 1, 1);
