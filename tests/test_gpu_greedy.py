@@ -53,6 +53,15 @@ def test_greedy_planted_full_size_workload():
     assert (got["row_argmax"][:vb.R] == vb.extra["planted"]).all()
 
 
+def test_greedy_more_rows_than_a_grid_dimension_holds():
+    """More than 65535 packed rows: the row-major stream grid is then one
+    dimensional (rows x chunks in x) instead of chunks x rows."""
+    sv = need_gpu()
+    vb = W.ragged_batch(seed=70, B=14000, k_max=8, V=64, dtype="f32")
+    assert vb.R > 65535
+    check_greedy(sv, vb)
+
+
 def test_greedy_neg_inf_rows_and_k_max_31():
     sv = need_gpu()
     vb = W.ragged_batch(seed=3, B=3, k_max=31, V=4099, dtype="f32", k_values=np.array([31, 0, 17]))
