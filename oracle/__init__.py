@@ -38,6 +38,7 @@ BAD_ROWS = 0x10
 BAD_SELECTED = 0x20
 BAD_RELAXED_K = 0x40
 BAD_BUDGET = 0x80
+BAD_MARGIN = 0x200
 
 
 def build(force: bool = False) -> str:
@@ -90,6 +91,9 @@ def lib():
         L.oracle_verify_relaxed.argtypes = [p, C.c_int, i64, i32, i32, i32, p, p, p,
                                             p, p, p, p, p]
         L.oracle_verify_relaxed.restype = u32
+        L.oracle_verify_margin.argtypes = [p, C.c_int, i64, i32, i32, i32, p, p, p, p, i32, i32,
+                                           p, i32, p, p, p, p, p]
+        L.oracle_verify_margin.restype = u32
         L.oracle_draft_confidence.argtypes = [p, C.c_int, i64, i32, i32, i32, p, f64, i32,
                                               p, p, p, p, p, p, p, p]
         L.oracle_draft_confidence.restype = u32
@@ -259,6 +263,39 @@ def verify_relaxed(logits, dtype, V, B, k_max, cu_rows, draft_ids, relaxed_k) ->
     Rr = max(int(cu[B]), 0)
     return VerifyResult(acc[:B], out[:B], nxt[:B], int(st),
                         dict(row_argmax=am[:Rr], row_rank=rk[:Rr]))
+
+
+# ----------------------------------------------------------------------------
+# Confidence-margin acceptance
+# ----------------------------------------------------------------------------
+
+def verify_margin(logits, dtype, V, B, k_max, cu_rows, draft_ids, margin, generated=None,
+                  from_position: int = 0, after_tokens: int = 0,
+                  protected_ids=None) -> VerifyResult:
+    """Greedy acceptance loosened by a logit margin (vSpec README §"启动"
+    approximate-acceptance preset, §"通用参数": --confidence-accept-margin,
+    --confidence-accept-from-position / --confidence-accept-after-tokens,
+    --confidence-protected-token-ids).  Draft d at position j of request b
+    passes when it is the first argmax, or when j >= from_position,
+    generated[b] + j >= after_tokens, d is not protected and the fp32 gap
+    max - z[d] <= margin[b].  Strict prefix; the emitted token is the
+    stopping row's first argmax."""
+    x, dt = _logits(logits, dtype)
+    cu = _c(cu_rows, np.int32); d = _c(draft_ids, np.int32)
+    mg = _c(margin, np.float32)
+    gen = None if generated is None else _c(generated, np.int32)
+    prot = np.zeros(1, np.int32) if protected_ids is None else _c(protected_ids, np.int32)
+    n_prot = 0 if protected_ids is None else int(prot.size)
+    R = max(int(cu[B]), 1)
+    acc, out, nxt = _outs(B, k_max)
+    am = np.zeros(R, np.int32); ok = np.zeros(R, np.int32)
+    st = lib().oracle_verify_margin(_ptr(x), dt, x.shape[1], V, B, k_max, _ptr(cu), _ptr(d),
+                                    _ptr(mg), _ptr(gen), int(from_position), int(after_tokens),
+                                    _ptr(prot), n_prot, _ptr(acc), _ptr(out), _ptr(nxt),
+                                    _ptr(am), _ptr(ok))
+    Rr = max(int(cu[B]), 0)
+    return VerifyResult(acc[:B], out[:B], nxt[:B], int(st),
+                        dict(row_argmax=am[:Rr], row_ok=ok[:Rr]))
 
 
 # ----------------------------------------------------------------------------

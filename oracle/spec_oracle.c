@@ -43,6 +43,9 @@
  *     optional global row budget keeps the top (G-B) entries ordered by
  *     (cumulative confidence desc, request asc, position asc).
  *   - NaN and +inf logits are outside the contract; -inf is allowed.
+ *   - confidence margin: the gap max - z[d] is taken in fp32 (the inputs
+ *     are exact fp32 values); position j of request b is eligible when
+ *     j >= from_position and generated[b] + j >= after_tokens.
  *
  * Parity pins for every function live in tests/test_oracle_*.py.
  */
@@ -63,6 +66,7 @@
 #define OR_BAD_SELECTED    0x20u
 #define OR_BAD_RELAXED_K   0x40u
 #define OR_BAD_BUDGET      0x80u
+#define OR_BAD_MARGIN      0x200u
 
 /* ------------------------------------------------------------------------ */
 /* threads                                                                  */
@@ -512,6 +516,71 @@ uint32_t oracle_verify_relaxed(const void *logits, int dtype, int64_t ld, int32_
         if (row_rank) row_rank[r] = rank[r];
     }
     free(amax); free(rank);
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Confidence-margin acceptance [vSpec §"启动", §"通用参数"]                  */
+/* ------------------------------------------------------------------------ */
+
+static int is_protected(int32_t d, const int32_t *ids, int32_t n)
+{
+    for (int32_t i = 0; i < n; ++i)
+        if (ids[i] == d) return 1;
+    return 0;
+}
+
+/* Greedy acceptance loosened by a logit margin: a draft is accepted when it
+   is the target's first argmax, or -- at an eligible position, for a token
+   outside the protected set -- when its logit lies within margin[b] of the
+   row maximum.  The prefix stays strict and the emitted token of the first
+   rejected row (or the bonus row) is that row's first argmax, as in greedy
+   verification.  row_ok[r] = 1 where the draft of row r passes. */
+uint32_t oracle_verify_margin(const void *logits, int dtype, int64_t ld, int32_t V,
+                              int32_t B, int32_t k_max, const int32_t *cu_rows,
+                              const int32_t *draft_ids, const float *margin,
+                              const int32_t *generated, int32_t from_position,
+                              int32_t after_tokens, const int32_t *protected_ids,
+                              int32_t n_protected,
+                              int32_t *accepted_len, int32_t *out_tokens, int32_t *next_token,
+                              int32_t *row_argmax, int32_t *row_ok)
+{
+    uint32_t status = 0;
+    int32_t R = total_rows_of(cu_rows, B);
+    int32_t n = R > 0 ? R : 1;
+    int32_t *amax = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    double *mx = (double *)malloc(sizeof(double) * (size_t)n);
+    int32_t *ok = (int32_t *)calloc((size_t)n, sizeof(int32_t));
+    oracle_row_reduce(logits, dtype, ld, V, R, mx, NULL, amax);
+    for (int32_t b = 0; b < B; ++b) {
+        int32_t k = request_k(cu_rows, b, k_max);
+        if (k < 0) { status |= OR_BAD_ROWS; emit_invalid(b, k_max, accepted_len, out_tokens, next_token); continue; }
+        float mg = margin[b];
+        if (isnan(mg)) status |= OR_BAD_MARGIN;
+        const int32_t r0 = cu_rows[b];
+        const int32_t gen = generated ? generated[b] : 0;
+        for (int32_t j = 0; j < k; ++j) {
+            const int32_t r = r0 + j, d = draft_ids[r];
+            if (d < 0 || d >= V) continue;
+            if (d == amax[r]) { ok[r] = 1; continue; }
+            if (isnan(mg) || j < from_position || (int64_t)gen + j < (int64_t)after_tokens) continue;
+            if (is_protected(d, protected_ids, n_protected)) continue;
+            /* both values are exact in fp32; the gap is rounded to fp32 */
+            const float m32 = (float)mx[r];
+            const float zd = (float)logit_at(logits, dtype, ld, r, d);
+            const float gap = m32 - zd;
+            if (gap <= mg) ok[r] = 1;
+        }
+        int32_t a = 0;
+        while (a < k && ok[r0 + a])
+            ++a;
+        emit(b, k_max, a, &draft_ids[r0], amax[r0 + a], accepted_len, out_tokens, next_token);
+    }
+    for (int32_t r = 0; r < R; ++r) {
+        if (row_argmax) row_argmax[r] = amax[r];
+        if (row_ok) row_ok[r] = ok[r];
+    }
+    free(amax); free(mx); free(ok);
     return status;
 }
 
