@@ -88,6 +88,7 @@ typedef enum {
 #define SPEC_STATUS_BAD_RELAXED_K   0x40u  /* relaxed K < 1: treated as 1                      */
 #define SPEC_STATUS_BAD_BUDGET      0x80u  /* max_rows < B: budget ignored                     */
 #define SPEC_STATUS_TIMEOUT         0x100u /* an on-chip copy wait gave up; results invalid    */
+#define SPEC_STATUS_BAD_MARGIN      0x200u /* confidence margin NaN: request verified strictly */
 
 /* A ragged batch of packed verify rows (all pointers device memory). */
 typedef struct {
@@ -191,6 +192,44 @@ SPEC_API int spec_verify_greedy_noalloc(const spec_batch *batch, const spec_outp
 SPEC_API int spec_verify_relaxed_topk(const spec_batch *batch, const int32_t *relaxed_k,
                              const spec_outputs *out, void *workspace,
                              size_t workspace_bytes, spec_stream stream);
+
+/*
+ * Greedy verification loosened by a confidence margin (vSpec README §"启动"
+ * approximate-acceptance preset; §"通用参数": --confidence-accept-margin,
+ * --confidence-accept-from-position / --confidence-accept-after-tokens,
+ * --confidence-protected-token-ids).  The result is no longer guaranteed to
+ * equal target-only greedy decoding.  Draft d at position j of request b
+ * (row r = cu_rows[b] + j, j < k_b) is accepted iff d is in [0, V) and
+ *   d == argmax(row r)  (first argmax: the strict rule always applies), or
+ *   j >= from_position, generated[b] + j >= after_tokens, d is not in
+ *   protected_ids, and max(row r) - z_r[d] <= margin[b] with the difference
+ *   rounded to fp32 (both values are exact in fp32).
+ * Acceptance stops at the first failure; the token emitted after the prefix
+ * is that row's first argmax.  A negative margin keeps request b strict; a
+ * NaN margin does too and sets SPEC_STATUS_BAD_MARGIN.
+ * Inputs (device memory, owned by the caller, read only):
+ *   margin         [B] f32 logit margins; required.
+ *   generated      [B] i32 tokens request b produced before this step, or
+ *                  NULL (all 0).
+ *   protected_ids  [n_protected] i32 token ids the margin never accepts, in
+ *                  any order; NULL when n_protected = 0.  Each draft row
+ *                  scans the list once (n_protected / 32 loads per lane).
+ * Returns SPEC_ERR_INVALID_ARG before any launch for a NULL margin,
+ * n_protected < 0, or n_protected > 0 with a NULL list.  Workspace as for
+ * spec_verify_greedy.
+ */
+typedef struct {
+    const float *margin;
+    const int32_t *generated;
+    const int32_t *protected_ids;
+    int32_t n_protected;
+    int32_t from_position;
+    int32_t after_tokens;
+} spec_margin;
+
+SPEC_API int spec_verify_greedy_margin(const spec_batch *batch, const spec_margin *margin,
+                                       const spec_outputs *out, void *workspace,
+                                       size_t workspace_bytes, spec_stream stream);
 
 /*
  * A1 + A3 + A4: stochastic verification with a point-mass draft (xLLM

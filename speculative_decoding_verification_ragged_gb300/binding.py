@@ -30,10 +30,11 @@ STATUS_BAD_SELECTED = 0x20
 STATUS_BAD_RELAXED_K = 0x40
 STATUS_BAD_BUDGET = 0x80
 STATUS_TIMEOUT = 0x100
+STATUS_BAD_MARGIN = 0x200
 
 EXPORTS = ["spec_workspace_bytes", "spec_draft_workspace_bytes", "spec_verify_greedy",
            "spec_verify_greedy_noalloc", "spec_verify_relaxed_topk",
-           "spec_verify_sample", "spec_draft_confidence", "spec_prefix_stats",
+           "spec_verify_greedy_margin", "spec_verify_sample", "spec_draft_confidence", "spec_prefix_stats",
            "spec_result_string", "spec_last_cuda_error", "spec_abi_version"]
 
 
@@ -58,6 +59,12 @@ class Sampling(C.Structure):
     _fields_ = [("temperature", C.c_void_p), ("top_k", C.c_void_p), ("top_p", C.c_void_p),
                 ("min_p", C.c_void_p), ("seed", C.c_void_p), ("request_id", C.c_void_p),
                 ("step", C.c_uint32)]
+
+
+class Margin(C.Structure):
+    _fields_ = [("margin", C.c_void_p), ("generated", C.c_void_p),
+                ("protected_ids", C.c_void_p), ("n_protected", C.c_int32),
+                ("from_position", C.c_int32), ("after_tokens", C.c_int32)]
 
 
 class Draft(C.Structure):
@@ -94,13 +101,15 @@ def load_library(path: Optional[str] = None) -> C.CDLL:
     L.spec_verify_greedy_noalloc.argtypes = [C.POINTER(Batch), C.POINTER(Outputs), vp]
     L.spec_verify_relaxed_topk.argtypes = [C.POINTER(Batch), vp, C.POINTER(Outputs), vp,
                                            C.c_size_t, vp]
+    L.spec_verify_greedy_margin.argtypes = [C.POINTER(Batch), C.POINTER(Margin),
+                                            C.POINTER(Outputs), vp, C.c_size_t, vp]
     L.spec_verify_sample.argtypes = [C.POINTER(Batch), C.POINTER(Sampling), C.POINTER(Outputs),
                                      vp, C.c_size_t, vp]
     L.spec_draft_confidence.argtypes = [C.POINTER(Draft), C.POINTER(Allocation), vp, C.c_size_t,
                                         vp]
     L.spec_prefix_stats.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp]
     for f in ["spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_relaxed_topk",
-              "spec_verify_sample",
+              "spec_verify_greedy_margin", "spec_verify_sample",
               "spec_draft_confidence", "spec_prefix_stats", "spec_abi_version"]:
         getattr(L, f).restype = C.c_int
     L.spec_result_string.argtypes = [C.c_int]
@@ -251,6 +260,29 @@ def verify_relaxed_topk(logits, cu_rows, draft_ids, relaxed_k, *, V: int, B: int
     o, res = _outputs(B, k_max, R_cap, logits.device, rows, stats)
     _check(L.spec_verify_relaxed_topk(C.byref(b), _dev(relaxed_k, "relaxed_k", torch.int32),
                                       C.byref(o), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return res
+
+
+def verify_greedy_margin(logits, cu_rows, draft_ids, margin, generated=None, protected_ids=None,
+                         from_position: int = 0, after_tokens: int = 0, *, V: int, B: int,
+                         k_max: int, R_cap: Optional[int] = None, workspace=None,
+                         rows: bool = True, stats=None, stream=None) -> dict:
+    """spec_verify_greedy_margin: greedy acceptance that also passes a draft
+    within margin[b] of the row maximum at eligible positions, never for a
+    protected token id; strict prefix."""
+    L = load_library()
+    R_cap = R_cap or B * (k_max + 1)
+    ws = workspace if workspace is not None else new_workspace(
+        R_cap, B, V, _logits_dtype(logits), logits.device)
+    b = _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids)
+    o, res = _outputs(B, k_max, R_cap, logits.device, rows, stats)
+    n_prot = 0 if protected_ids is None else int(protected_ids.numel())
+    m = Margin(_dev(margin, "margin", torch.float32),
+               _dev(generated, "generated", torch.int32),
+               _dev(protected_ids, "protected_ids", torch.int32) if n_prot else None,
+               n_prot, int(from_position), int(after_tokens))
+    _check(L.spec_verify_greedy_margin(C.byref(b), C.byref(m), C.byref(o), ws.data_ptr(),
+                                       ws.numel(), _stream(stream)))
     return res
 
 

@@ -36,6 +36,11 @@ struct VerifyParams {
     uint32_t step;
     // relaxed top-K
     const int32_t *relaxed_k;
+    // greedy with a confidence margin (margin == nullptr: strict greedy)
+    const float *margin;
+    const int32_t *generated;
+    const int32_t *protected_ids;
+    int32_t n_protected, from_position, after_tokens;
     // draft confidence (MODE_CONF: rows are draft positions)
     const int32_t *selected;
     float *conf;

@@ -666,6 +666,28 @@ __global__ void __launch_bounds__(256) row_info_kernel(const VerifyParams p, int
         inf.seed_hi = static_cast<uint32_t>(sd >> 32);
         inf.rid = p.request_id ? __ldg(p.request_id + b) : static_cast<uint32_t>(b);
     }
+    if (MODE == MODE_GREEDY && p.margin) {
+        // the margin applies to a draft row at an eligible position whose
+        // draft is in the vocabulary and not protected; elsewhere zd is NaN,
+        // which fails the gap test in the finish
+        const float mg = __ldg(p.margin + b);
+        if (isnan(mg)) inf.bad |= SPEC_STATUS_BAD_MARGIN;
+        const int32_t gen = p.generated ? __ldg(p.generated + b) : 0;
+        const int32_t d = inf.draft;
+        bool elig = inf.valid && inf.pos < inf.k_b && d >= 0 && d < p.V && !isnan(mg) &&
+                    inf.pos >= p.from_position &&
+                    static_cast<int64_t>(gen) + inf.pos >= static_cast<int64_t>(p.after_tokens);
+        if (elig && p.n_protected > 0) {
+            bool hit = false;
+            for (int i = lane; i < p.n_protected; i += 32) hit |= (__ldg(p.protected_ids + i) == d);
+            elig = !__any_sync(0xFFFFFFFFu, hit);
+        }
+        inf.zd = __int_as_float(0x7FC00000);
+        if (elig) {
+            const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
+            inf.zd = E::load(row, d);
+        }
+    }
     if (MODE == MODE_RELAXED) {
         int32_t K = __ldg(p.relaxed_k + b);
         if (K < 1) { inf.bad |= SPEC_STATUS_BAD_RELAXED_K; K = 1; }
@@ -1217,7 +1239,8 @@ __device__ __forceinline__ void request_chain(const VerifyParams &p, const RowIn
     const int32_t yj = (j <= k) ? __ldcg(p.ws_tok + r0 + j) : -1;
     const int32_t dj = (j < k) ? __ldg(p.draft_ids + r0 + j) : -1;
     bool ok;
-    if (MODE == MODE_RELAXED) ok = (j < k) && __ldcg(p.ws_flag + r0 + j) != 0;
+    if (MODE == MODE_RELAXED || (MODE == MODE_GREEDY && p.margin))
+        ok = (j < k) && __ldcg(p.ws_flag + r0 + j) != 0;
     else ok = (j < k) && (yj == dj);
     const unsigned mism = __ballot_sync(0xFFFFFFFFu, (j < k) && !ok);
     const int a = mism ? (__ffs(mism) - 1) : k;
@@ -1388,6 +1411,9 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
     int32_t flag = 0;
     if (MODE == MODE_RELAXED)
         flag = (info.draft >= 0 && info.draft < p.V && sh.CNT < info.K) ? 1 : 0;
+    // margin: the first argmax, or a gap max - z[d] (fp32) within the margin
+    if (MODE == MODE_GREEDY && p.margin)
+        flag = (info.draft == AMAX || M - info.zd <= __ldg(p.margin + info.b)) ? 1 : 0;
 
     HeavyRec hrec = {};                    // thread 0: the queued row's record
     if (MODE == MODE_SAMPLE && info.T > 0.f && M > -INFINITY) {
@@ -1700,7 +1726,7 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
         } else if (!queued) {
             if (p.row_token) p.row_token[r] = y;
             p.ws_tok[r] = y;
-            if (MODE == MODE_RELAXED) p.ws_flag[r] = flag;
+            if (MODE == MODE_RELAXED || (MODE == MODE_GREEDY && p.margin)) p.ws_flag[r] = flag;
         }
     }
     if (MODE != MODE_CONF && !queued && warp == 0) request_chain<MODE>(p, info, r);

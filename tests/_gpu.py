@@ -44,6 +44,15 @@ def run_relaxed(sv, vb: W.VerifyBatch, K, **kw):
                                   k_max=vb.k_max, R_cap=vb.logits.shape[0], **kw)
 
 
+def run_margin(sv, vb: W.VerifyBatch, margin, generated=None, protected_ids=None, **kw):
+    return sv.verify_greedy_margin(
+        logits_tensor(vb.logits, vb.dtype), t(vb.cu_rows), t(vb.draft_ids),
+        t(np.asarray(margin, np.float32)),
+        t(np.asarray(generated, np.int32)) if generated is not None else None,
+        t(np.asarray(protected_ids, np.int32)) if protected_ids is not None else None,
+        V=vb.V, B=vb.B, k_max=vb.k_max, R_cap=vb.logits.shape[0], **kw)
+
+
 def run_sample(sv, vb: W.VerifyBatch, p: W.SampleParams, **kw):
     return sv.verify_sample(logits_tensor(vb.logits, vb.dtype), t(vb.cu_rows), t(vb.draft_ids),
                             t(p.temperature), t(p.top_k), t(p.top_p), t(p.min_p), t(p.seed),

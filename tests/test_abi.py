@@ -37,6 +37,12 @@ def test_library_exports_every_declared_symbol(sv):
     assert L.spec_abi_version() == 100
 
 
+def test_package_exposes_a_binding_per_entry_point(sv):
+    for name in sv.EXPORTS:
+        if name.startswith("spec_verify_") or name in ("spec_draft_confidence", "spec_prefix_stats"):
+            assert callable(getattr(sv, name[len("spec_"):])), name
+
+
 def test_workspace_bytes(sv):
     L = sv.load_library()
     # 640 rows of V = 152064 bf16: 10 chunks of 32 KiB per row
@@ -85,6 +91,13 @@ def test_host_argument_errors_launch_nothing(sv):
     s = Sampling(fake, None, fake, fake, fake, None, 0)
     assert L.spec_verify_sample(C.byref(b), C.byref(s), C.byref(outs), ws, n, None) == 1
     assert L.spec_verify_relaxed_topk(C.byref(b), None, C.byref(outs), ws, n, None) == 1
+    from speculative_decoding_verification_ragged_gb300.binding import Margin
+    for m, rc in [(Margin(None, None, None, 0, 0, 0), 1), (Margin(fake, None, None, -1, 0, 0), 1),
+                  (Margin(fake, None, None, 3, 0, 0), 1)]:
+        assert L.spec_verify_greedy_margin(C.byref(b), C.byref(m), C.byref(outs), ws, n, None) == rc
+    m = Margin(fake, None, fake, 3, 1, 4)
+    assert L.spec_verify_greedy_margin(C.byref(b), C.byref(m), C.byref(outs), ws, n - 1, None) == 4
+    assert L.spec_verify_greedy_margin(C.byref(b), None, C.byref(outs), ws, n, None) == 1
     assert L.spec_prefix_stats(fake, fake, 4, 40, fake, fake, None, None, None) == 2
     assert L.spec_prefix_stats(fake, fake, 0, 4, fake, fake, None, None, None) == 1
     assert L.spec_result_string(4) == b"SPEC_ERR_WORKSPACE"

@@ -1,12 +1,13 @@
-"""GPU parity (through the C ABI) of the fused row reduction, greedy and
-relaxed top-K verification and the prefix-acceptance counters against the
-CPU oracle.  Integers bit-exact; LSE within 1e-5 relative (fp32 vs fp64)."""
+"""GPU parity (through the C ABI) of the fused row reduction, greedy,
+margin-loosened greedy and relaxed top-K verification and the
+prefix-acceptance counters against the CPU oracle.  Integers bit-exact; LSE within 1e-5 relative (fp32 vs fp64)."""
 import numpy as np
 import pytest
 
 import oracle
 import workloads as W
-from tests._gpu import assert_requests_equal, host, need_gpu, run_greedy, run_relaxed, t, torch
+from tests._gpu import (assert_requests_equal, host, need_gpu, run_greedy, run_margin,
+                        run_relaxed, t, torch)
 
 pytestmark = pytest.mark.gpu
 
@@ -136,6 +137,58 @@ def test_relaxed_eagle_workload_with_fused_stats():
     torch.cuda.synchronize()
     for a, b in [(acc, racc), (ver, rver), (hist, rhist), (acc2, racc), (ver2, rver),
                  (hist2, rhist)]:
+        np.testing.assert_array_equal(a.cpu().numpy(), b)
+
+
+@pytest.mark.parametrize("dtype,V,ld", [("bf16", 50_000, 50_003), ("f32", 33_001, 33_001),
+                                        ("bf16", 40, 40)])
+def test_margin_ragged_with_positions_and_protected_ids(dtype, V, ld):
+    """Per-request margins (0, small, the 5.25 preset, infinite, negative,
+    NaN), a first eligible position, a count of generated tokens and a
+    protected list longer than a warp, over drafts near the top values."""
+    sv = need_gpu()
+    base = W.ragged_batch(seed=40 + V % 7, B=12, k_max=7, V=V, dtype=dtype, ld=ld, tie_top=True)
+    vb = W.near_top_drafts(base, seed=41)
+    margin = np.array([0, 0.5, 1, 2, 5.25, np.inf, -1, np.nan, 3, 5.25, 1.5, 0.25], np.float32)
+    gen = np.array([0, 9, 2, 0, 5, 1, 0, 3, 4, 8, 0, 6], np.int32)
+    rng = np.random.default_rng(42)
+    drafts = vb.draft_ids[vb.draft_ids >= 0]
+    prot = np.concatenate([rng.choice(drafts, size=min(10, drafts.size), replace=False),
+                           rng.integers(0, V, size=60)]).astype(np.int32)
+    for kw in [dict(), dict(from_position=1, after_tokens=4), dict(from_position=3)]:
+        for g, pr in [(None, None), (gen, prot)]:
+            ref = oracle.verify_margin(vb.logits, vb.dtype, vb.V, vb.B, vb.k_max, vb.cu_rows,
+                                       vb.draft_ids, margin, generated=g, protected_ids=pr, **kw)
+            got = host(run_margin(sv, vb, margin, g, pr, **kw))
+            assert_requests_equal(got, ref)
+            np.testing.assert_array_equal(got["row_argmax"][:vb.R], ref.rows["row_argmax"])
+            assert got["status"][0] == ref.status == 0x200
+
+
+def test_margin_preset_full_size_with_fused_stats():
+    """The approximate-acceptance preset: margin 5.25 for every request on
+    B=128, k=4, V=152064 bf16 rows with drafts among the top 2000 values
+    (gaps on both sides of the margin); the fused counters match the
+    oracle's accepted lengths."""
+    sv = need_gpu()
+    dev = "cuda"
+    vb = W.near_top_drafts(W.ragged_batch(seed=W.data_seed(2, 7), B=128, k_max=4, V=152064,
+                                          k_values=np.full(128, 4)), seed=43, max_rank=2000)
+    margin = np.full(vb.B, 5.25, np.float32)
+    ref = oracle.verify_margin(vb.logits, vb.dtype, vb.V, vb.B, vb.k_max, vb.cu_rows,
+                               vb.draft_ids, margin)
+    greedy = oracle.verify_greedy(vb.logits, vb.dtype, vb.V, vb.B, vb.k_max, vb.cu_rows,
+                                  vb.draft_ids)
+    # the margin decides: more than greedy accepts, fewer than every draft
+    assert greedy.accepted_len.sum() < ref.accepted_len.sum() < vb.B * vb.k_max
+    acc = torch.zeros(4, dtype=torch.int64, device=dev)
+    ver = torch.zeros(4, dtype=torch.int64, device=dev)
+    hist = torch.zeros(5, dtype=torch.int64, device=dev)
+    got = host(run_margin(sv, vb, margin, stats=(acc, ver, hist)))
+    assert_requests_equal(got, ref)
+    assert got["status"][0] == ref.status == 0
+    racc, rver, rhist, _ = oracle.prefix_stats(ref.accepted_len, vb.cu_rows, vb.B, vb.k_max)
+    for a, b in [(acc, racc), (ver, rver), (hist, rhist)]:
         np.testing.assert_array_equal(a.cpu().numpy(), b)
 
 

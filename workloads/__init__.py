@@ -351,3 +351,24 @@ def ragged_batch(seed: int, B: int, k_max: int, V: int, dtype: str = "bf16",
     if R:
         d[cu[1:] - 1] = -1
     return VerifyBatch(enc, dtype, V, B, k_max, cu, d)
+
+
+def near_top_drafts(vb: VerifyBatch, seed: int, p_top: float = 0.4,
+                    max_rank: int = 10) -> VerifyBatch:
+    """The same rows with each draft replaced by the token at a random rank
+    among its row's largest values: rank 0 (the first top value) with
+    probability p_top, else a rank uniform in [1, max_rank] (value order,
+    lower index first on equal values).  Drafts then sit at small, varied
+    distances below the row maximum, the range a confidence margin decides."""
+    rng = np.random.default_rng(seed)
+    vals = bf16_bits_to_f32(vb.logits) if vb.dtype == "bf16" else vb.logits
+    d = vb.draft_ids.copy()
+    for b in range(vb.B):
+        for r in range(int(vb.cu_rows[b]), int(vb.cu_rows[b + 1]) - 1):
+            q = 0 if rng.random() < p_top else int(rng.integers(1, max_rank + 1))
+            q = min(q, vb.V - 1)
+            v = vals[r, :vb.V]
+            cut = np.partition(v, vb.V - 1 - q)[vb.V - 1 - q]      # the (q+1)-th largest
+            idx = np.nonzero(v >= cut)[0]
+            d[r] = idx[np.argsort(-v[idx], kind="stable")][q]
+    return VerifyBatch(vb.logits, vb.dtype, vb.V, vb.B, vb.k_max, vb.cu_rows, d)
