@@ -365,6 +365,23 @@ def time_entry_points(sv, dev, stream, args) -> dict:
     out["spec_verify_greedy"] = {"workload": "B=128 k=4 V=152064 bf16 planted, with row max/LSE/argmax",
                                  "rows": vb.R, "us": round(ms * 1e3, 2),
                                  "hbm_gbs": round(vb.R * vb.V * 2 / (ms * 1e-3) / 1e9, 1)}
+    # the same rows with the 5.25 confidence margin, positions from 1, and 16
+    # protected token ids
+    mg = torch.full((vb.B,), 5.25, dtype=torch.float32, device=dev)
+    prot = torch.arange(151_643, 151_659, dtype=torch.int32, device=dev)
+    m = Bd.Margin(mg.data_ptr(), None, prot.data_ptr(), prot.numel(), 1, 0)
+
+    def margin(i):
+        b.logits = sets[i % len(sets)].data_ptr()
+        ok(L.spec_verify_greedy_margin(C.byref(b), C.byref(m), C.byref(o), ws.data_ptr(),
+                                       ws.numel(), s))
+    for i in range(5):
+        margin(i)
+    ms = _time_launches(margin, n, stream)
+    out["spec_verify_greedy_margin"] = {
+        "workload": "B=128 k=4 V=152064 bf16 planted, margin 5.25 from position 1, 16 protected ids",
+        "rows": vb.R, "us": round(ms * 1e3, 2),
+        "hbm_gbs": round(vb.R * vb.V * 2 / (ms * 1e-3) / 1e9, 1)}
     del sets
     # relaxed top-K (EAGLE-relaxed, B=256, k=5, V=152064, K=4)
     vb = W.relaxed_planted()
