@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "libspecverify.so")
-SOURCES = ["verify.cu", "draft.cu", "capi.cu"]
+SOURCES = ["verify.cu", "draft.cu", "capi.cu", "step_policy.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -26,8 +26,8 @@ def _stale() -> bool:
     if not os.path.exists(OUT):
         return True
     t = os.path.getmtime(OUT)
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "spec_verify.h"),
-                                                                  os.path.abspath(__file__)]
+    deps = ([os.path.join(CSRC, f) for f in os.listdir(CSRC)] +
+            [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)] + [os.path.abspath(__file__)])
     return any(os.path.getmtime(d) > t for d in deps)
 
 
@@ -42,7 +42,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
                      "-Xcompiler", "-fvisibility=hidden"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(objdir, src.replace(".cu", ".o"))
+        obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")
         cmd = [cc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

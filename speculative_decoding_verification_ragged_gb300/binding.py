@@ -11,6 +11,7 @@ import ctypes as C
 import os
 from typing import Optional
 
+import numpy as np
 import torch
 
 from . import _build
@@ -35,7 +36,9 @@ STATUS_BAD_MARGIN = 0x200
 EXPORTS = ["spec_workspace_bytes", "spec_draft_workspace_bytes", "spec_verify_greedy",
            "spec_verify_greedy_noalloc", "spec_verify_relaxed_topk",
            "spec_verify_greedy_margin", "spec_verify_sample", "spec_draft_confidence", "spec_prefix_stats",
-           "spec_result_string", "spec_last_cuda_error", "spec_abi_version"]
+           "spec_result_string", "spec_last_cuda_error", "spec_abi_version",
+           "spec_step_state_bytes", "spec_step_init", "spec_step_update", "spec_step_query",
+           "spec_step_cost_sps", "spec_step_cost_additive"]
 
 
 class SpecError(RuntimeError):
@@ -65,6 +68,12 @@ class Margin(C.Structure):
     _fields_ = [("margin", C.c_void_p), ("generated", C.c_void_p),
                 ("protected_ids", C.c_void_p), ("n_protected", C.c_int32),
                 ("from_position", C.c_int32), ("after_tokens", C.c_int32)]
+
+
+class StepPolicy(C.Structure):
+    _fields_ = [("k_min", C.c_int32), ("k_max", C.c_int32), ("k_init", C.c_int32),
+                ("window_size", C.c_int32), ("update_interval", C.c_int32),
+                ("switch_min_gain", C.c_double)]
 
 
 class Draft(C.Structure):
@@ -111,6 +120,16 @@ def load_library(path: Optional[str] = None) -> C.CDLL:
     for f in ["spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_relaxed_topk",
               "spec_verify_greedy_margin", "spec_verify_sample",
               "spec_draft_confidence", "spec_prefix_stats", "spec_abi_version"]:
+        getattr(L, f).restype = C.c_int
+    L.spec_step_state_bytes.restype = C.c_size_t
+    L.spec_step_state_bytes.argtypes = []
+    L.spec_step_init.argtypes = [vp, C.c_size_t, C.POINTER(StepPolicy)]
+    L.spec_step_update.argtypes = [vp, vp, vp, vp, i32, vp]
+    L.spec_step_query.argtypes = [vp, vp, vp, vp]
+    L.spec_step_cost_sps.argtypes = [i32, i32, vp, vp, i32, vp]
+    L.spec_step_cost_additive.argtypes = [i32, i32, C.c_double, vp, vp, i32, vp, vp, i32, vp]
+    for f in ["spec_step_init", "spec_step_update", "spec_step_query", "spec_step_cost_sps",
+              "spec_step_cost_additive"]:
         getattr(L, f).restype = C.c_int
     L.spec_result_string.argtypes = [C.c_int]
     L.spec_result_string.restype = C.c_char_p
@@ -392,3 +411,79 @@ class PreparedSample:
         if rc:
             _check(rc)
         return self.res
+
+
+# ------------------------------------------------------------------------
+# adaptive draft-step controller (host code in the library; no GPU needed)
+# ------------------------------------------------------------------------
+
+def _host(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(C.c_void_p)
+
+
+class StepController:
+    """spec_step_init / spec_step_update / spec_step_query: one speculative
+    step count per batch from the windowed prefix acceptance of completed
+    batches and the full-step cost of each candidate."""
+
+    def __init__(self, k_min: int, k_max: int, k_init: int, window_size: int = 20,
+                 update_interval: int = 5, switch_min_gain: float = 0.05):
+        L = load_library()
+        self.k_max = k_max
+        self._state = np.zeros((L.spec_step_state_bytes() + 7) // 8, np.uint64)
+        pol = StepPolicy(k_min, k_max, k_init, window_size, update_interval, switch_min_gain)
+        _check(L.spec_step_init(self._state.ctypes.data_as(C.c_void_p), self._state.nbytes,
+                                C.byref(pol)))
+
+    def update(self, acc, ver, cost_ms, B: int) -> int:
+        L = load_library()
+        a, pa = _host(acc, np.int64)
+        v, pv = _host(ver, np.int64)
+        c, pc = _host(cost_ms, np.float64)
+        k = C.c_int32(0)
+        _check(L.spec_step_update(self._state.ctypes.data_as(C.c_void_p), pa, pv, pc, int(B),
+                                  C.byref(k)))
+        return int(k.value)
+
+    def query(self):
+        """(prefix_acceptance [k_max], score [k_max + 1], current k)."""
+        L = load_library()
+        pa = np.zeros(max(self.k_max, 1), np.float64)
+        sc = np.zeros(self.k_max + 1, np.float64)
+        k = C.c_int32(0)
+        _check(L.spec_step_query(self._state.ctypes.data_as(C.c_void_p),
+                                 pa.ctypes.data_as(C.c_void_p), sc.ctypes.data_as(C.c_void_p),
+                                 C.byref(k)))
+        return pa[:self.k_max], sc, int(k.value)
+
+
+def step_cost_sps(B: int, k_max: int, g_rows, sps) -> np.ndarray:
+    """spec_step_cost_sps: cost_ms[k] = 1000 / SPS of the first captured
+    graph size >= B (k + 1), +inf when none covers it."""
+    L = load_library()
+    g, pg = _host(g_rows, np.int32)
+    s_, ps = _host(sps, np.float64)
+    if g.size != s_.size:
+        raise SpecError("g_rows and sps differ in length")
+    out = np.zeros(k_max + 1, np.float64)
+    _check(L.spec_step_cost_sps(int(B), int(k_max), pg, ps, int(g.size),
+                                out.ctypes.data_as(C.c_void_p)))
+    return out
+
+
+def step_cost_additive(B: int, k_max: int, bias_s: float, b_buckets, alpha_s, g_rows,
+                       theta_s) -> np.ndarray:
+    """spec_step_cost_additive: cost_ms[k] = 1000 (bias + alpha(Bcap) +
+    theta(G_k)) over the first covering request bucket and graph size."""
+    L = load_library()
+    b, pb = _host(b_buckets, np.int32)
+    a, pa = _host(alpha_s, np.float64)
+    g, pg = _host(g_rows, np.int32)
+    t, pt = _host(theta_s, np.float64)
+    if b.size != a.size or g.size != t.size:
+        raise SpecError("bucket and term lists differ in length")
+    out = np.zeros(k_max + 1, np.float64)
+    _check(L.spec_step_cost_additive(int(B), int(k_max), float(bias_s), pb, pa, int(b.size),
+                                     pg, pt, int(g.size), out.ctypes.data_as(C.c_void_p)))
+    return out
