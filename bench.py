@@ -306,6 +306,7 @@ def run_ours(args) -> None:
             for e in entries.values():
                 e["pct_of_peak"] = round(100 * e["hbm_gbs"] / peaks["hbm_gbs"], 1)
             line["entry_points"] = entries
+            line["step_controller"] = time_step_controller(sv)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(vb, p)
         print(json.dumps(line), flush=True)
@@ -439,6 +440,36 @@ def time_entry_points(sv, dev, stream, args) -> dict:
     ms = _time_launches(stats, n, stream)
     out["spec_prefix_stats"] = {"workload": "B=128 k=4", "us": round(ms * 1e3, 2), "hbm_gbs": 0.0}
     return out
+
+
+def time_step_controller(sv, batches: int = 20_000) -> dict:
+    """Host time of one spec_step_update (the adaptive draft-step decision)
+    with the page's policy (window 20, re-scoring every 5, gain 5 %), k <= 5,
+    B = 128 and an SPS cost table, fed the counters of synthetic batches."""
+    rng = np.random.default_rng(7)
+    ctl = sv.StepController(1, 5, 4)
+    cost = sv.step_cost_sps(128, 5, [128, 256, 512, 768], [60.0, 55.0, 45.0, 38.0])
+    ver = np.full(5, 128, np.int64)
+    accs = [np.sort(rng.integers(0, 129, size=5))[::-1].astype(np.int64) for _ in range(64)]
+    t0 = time.perf_counter()
+    for i in range(batches):
+        ctl.update(accs[i % 64], ver, cost, 128)
+    us = (time.perf_counter() - t0) / batches * 1e6
+    # the C call alone: arguments marshalled once
+    L = sv.load_library()
+    st = ctl._state.ctypes.data_as(ctypes.c_void_p)
+    pa = [a.ctypes.data_as(ctypes.c_void_p) for a in accs]
+    pv, pc, k = ver.ctypes.data_as(ctypes.c_void_p), cost.ctypes.data_as(ctypes.c_void_p), \
+        ctypes.c_int32(0)
+    kr = ctypes.byref(k)
+    fn = L.spec_step_update
+    t0 = time.perf_counter()
+    for i in range(batches):
+        fn(st, pa[i % 64], pv, pc, 128, kr)
+    us_c = (time.perf_counter() - t0) / batches * 1e6
+    return {"policy": "window 20, every 5 batches, gain 0.05, k in [1, 5], B=128, SPS costs",
+            "batches": batches, "us_per_batch_binding": round(us, 3),
+            "us_per_batch_c_call": round(us_c, 3), "k_final": int(k.value)}
 
 
 def cpu_baseline(vb, p, budget_s: float = 10.0) -> dict:

@@ -150,3 +150,12 @@ def test_abi_state_checks(sv):
     assert L.spec_step_update(p, acc.ctypes.data_as(C.c_void_p), ver.ctypes.data_as(C.c_void_p),
                               None, 4, C.byref(k)) == 0                   # not due: no costs
     assert k.value == 1
+
+
+def test_bench_times_the_controller_on_the_host(sv):
+    """The benchmark's controller timing runs without a GPU and ends on a
+    valid step."""
+    import bench
+    r = bench.time_step_controller(sv, batches=200)
+    assert r["batches"] == 200 and 1 <= r["k_final"] <= 5
+    assert r["us_per_batch_c_call"] > 0 and r["us_per_batch_binding"] > 0
