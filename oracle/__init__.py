@@ -91,6 +91,9 @@ def lib():
         L.oracle_verify_relaxed.argtypes = [p, C.c_int, i64, i32, i32, i32, p, p, p,
                                             p, p, p, p, p]
         L.oracle_verify_relaxed.restype = u32
+        L.oracle_verify_greedy_active.argtypes = [p, C.c_int, i64, i32, i32, i32, p, p, p,
+                                                  p, p, p, p, p]
+        L.oracle_verify_greedy_active.restype = u32
         L.oracle_verify_margin.argtypes = [p, C.c_int, i64, i32, i32, i32, p, p, p, p, i32, i32,
                                            p, i32, p, p, p, p, p]
         L.oracle_verify_margin.restype = u32
@@ -263,6 +266,32 @@ def verify_relaxed(logits, dtype, V, B, k_max, cu_rows, draft_ids, relaxed_k) ->
     Rr = max(int(cu[B]), 0)
     return VerifyResult(acc[:B], out[:B], nxt[:B], int(st),
                         dict(row_argmax=am[:Rr], row_rank=rk[:Rr]))
+
+
+# ----------------------------------------------------------------------------
+# Greedy verification over an active vocabulary
+# ----------------------------------------------------------------------------
+
+def verify_greedy_active(logits, dtype, V, B, k_max, cu_rows, draft_ids,
+                         vocab_ids) -> VerifyResult:
+    """Greedy verification when the target scores only V active columns,
+    column i standing for full token id vocab_ids[i] (vSpec README
+    §"EAGLE 功能", §"代码所有权": active-vocabulary LM head with a full
+    token-id map).  Row token = vocab_ids[first argmax column]; drafts are
+    full ids, accepted while equal to it."""
+    x, dt = _logits(logits, dtype)
+    cu = _c(cu_rows, np.int32); d = _c(draft_ids, np.int32); m = _c(vocab_ids, np.int32)
+    if m.size < V:
+        raise ValueError("vocab_ids needs one full id per active column")
+    R = max(int(cu[B]), 1)
+    acc, out, nxt = _outs(B, k_max)
+    col = np.zeros(R, np.int32); tok = np.zeros(R, np.int32)
+    st = lib().oracle_verify_greedy_active(_ptr(x), dt, x.shape[1], V, B, k_max, _ptr(cu),
+                                           _ptr(d), _ptr(m), _ptr(acc), _ptr(out), _ptr(nxt),
+                                           _ptr(col), _ptr(tok))
+    Rr = max(int(cu[B]), 0)
+    return VerifyResult(acc[:B], out[:B], nxt[:B], int(st),
+                        dict(row_argmax=col[:Rr], row_token=tok[:Rr]))
 
 
 # ----------------------------------------------------------------------------

@@ -520,6 +520,47 @@ uint32_t oracle_verify_relaxed(const void *logits, int dtype, int64_t ld, int32_
 }
 
 /* ------------------------------------------------------------------------ */
+/* Greedy verification over an active vocabulary [vSpec §"EAGLE 功能",      */
+/* §"代码所有权": active-vocabulary LM head with a full token-id map]        */
+/* ------------------------------------------------------------------------ */
+
+/* The target scores only V active columns; column i stands for the full
+   token id vocab_ids[i].  The row's token is the full id of its first
+   argmax column; drafts are full ids and are accepted while they equal it.
+   row_argmax[r] is the column, row_token[r] the full id. */
+uint32_t oracle_verify_greedy_active(const void *logits, int dtype, int64_t ld, int32_t V,
+                                     int32_t B, int32_t k_max, const int32_t *cu_rows,
+                                     const int32_t *draft_ids, const int32_t *vocab_ids,
+                                     int32_t *accepted_len, int32_t *out_tokens,
+                                     int32_t *next_token, int32_t *row_argmax,
+                                     int32_t *row_token)
+{
+    uint32_t status = 0;
+    int32_t R = total_rows_of(cu_rows, B);
+    int32_t n = R > 0 ? R : 1;
+    int32_t *col = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    int32_t *tok = (int32_t *)malloc(sizeof(int32_t) * (size_t)n);
+    oracle_row_reduce(logits, dtype, ld, V, R, NULL, NULL, col);
+    for (int32_t r = 0; r < R; ++r)
+        tok[r] = vocab_ids[col[r]];
+    for (int32_t b = 0; b < B; ++b) {
+        int32_t k = request_k(cu_rows, b, k_max);
+        if (k < 0) { status |= OR_BAD_ROWS; emit_invalid(b, k_max, accepted_len, out_tokens, next_token); continue; }
+        const int32_t r0 = cu_rows[b];
+        int32_t a = 0;
+        while (a < k && draft_ids[r0 + a] == tok[r0 + a])
+            ++a;
+        emit(b, k_max, a, &draft_ids[r0], tok[r0 + a], accepted_len, out_tokens, next_token);
+    }
+    for (int32_t r = 0; r < R; ++r) {
+        if (row_argmax) row_argmax[r] = col[r];
+        if (row_token) row_token[r] = tok[r];
+    }
+    free(col); free(tok);
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Confidence-margin acceptance [vSpec §"启动", §"通用参数"]                  */
 /* ------------------------------------------------------------------------ */
 
