@@ -194,6 +194,24 @@ SPEC_API int spec_verify_relaxed_topk(const spec_batch *batch, const int32_t *re
                              size_t workspace_bytes, spec_stream stream);
 
 /*
+ * Greedy verification over an active vocabulary (vSpec README §"EAGLE 功能",
+ * §"代码所有权": an active-vocabulary target LM head with a full token-id
+ * map).  The logits have batch->V columns; column i stands for the full
+ * token id vocab_ids[i].  A row's token is vocab_ids[first argmax column];
+ * draft_ids hold FULL token ids and are accepted while they equal the row's
+ * token; out_tokens and next_token are full ids.  Optional row outputs:
+ * row_argmax is the column, row_token the full id.  The page's active
+ * vocabulary presumes pure greedy decoding, so there is no sampling variant.
+ * vocab_ids: device [batch->V], read only; ids are copied as given (a full
+ * id outside the model's vocabulary is the caller's error).  Returns
+ * SPEC_ERR_INVALID_ARG before any launch for a NULL map.  Workspace as for
+ * spec_verify_greedy (with V = the active column count).
+ */
+SPEC_API int spec_verify_greedy_active(const spec_batch *batch, const int32_t *vocab_ids,
+                                       const spec_outputs *out, void *workspace,
+                                       size_t workspace_bytes, spec_stream stream);
+
+/*
  * Greedy verification loosened by a confidence margin (vSpec README §"启动"
  * approximate-acceptance preset; §"通用参数": --confidence-accept-margin,
  * --confidence-accept-from-position / --confidence-accept-after-tokens,

@@ -8,11 +8,11 @@ from ._build import build  # noqa: F401
 from .binding import (  # noqa: F401
     EXPORTS, SpecError, StepController, draft_confidence, load_library, new_workspace,
     prefix_stats, step_cost_additive, step_cost_sps,
-    verify_greedy, verify_greedy_margin, verify_greedy_noalloc, verify_relaxed_topk,
+    verify_greedy, verify_greedy_active, verify_greedy_margin, verify_greedy_noalloc, verify_relaxed_topk,
     verify_sample, workspace_bytes,
 )
 
 __all__ = ["build", "load_library", "new_workspace", "workspace_bytes", "verify_greedy",
-           "verify_greedy_noalloc", "verify_greedy_margin",
+           "verify_greedy_noalloc", "verify_greedy_margin", "verify_greedy_active",
            "verify_relaxed_topk", "verify_sample", "draft_confidence", "prefix_stats",
            "StepController", "step_cost_sps", "step_cost_additive", "SpecError", "EXPORTS"]

@@ -35,7 +35,7 @@ STATUS_BAD_MARGIN = 0x200
 
 EXPORTS = ["spec_workspace_bytes", "spec_draft_workspace_bytes", "spec_verify_greedy",
            "spec_verify_greedy_noalloc", "spec_verify_relaxed_topk",
-           "spec_verify_greedy_margin", "spec_verify_sample", "spec_draft_confidence", "spec_prefix_stats",
+           "spec_verify_greedy_margin", "spec_verify_greedy_active", "spec_verify_sample", "spec_draft_confidence", "spec_prefix_stats",
            "spec_result_string", "spec_last_cuda_error", "spec_abi_version",
            "spec_step_state_bytes", "spec_step_init", "spec_step_update", "spec_step_query",
            "spec_step_cost_sps", "spec_step_cost_additive"]
@@ -110,6 +110,8 @@ def load_library(path: Optional[str] = None) -> C.CDLL:
     L.spec_verify_greedy_noalloc.argtypes = [C.POINTER(Batch), C.POINTER(Outputs), vp]
     L.spec_verify_relaxed_topk.argtypes = [C.POINTER(Batch), vp, C.POINTER(Outputs), vp,
                                            C.c_size_t, vp]
+    L.spec_verify_greedy_active.argtypes = [C.POINTER(Batch), vp, C.POINTER(Outputs), vp,
+                                            C.c_size_t, vp]
     L.spec_verify_greedy_margin.argtypes = [C.POINTER(Batch), C.POINTER(Margin),
                                             C.POINTER(Outputs), vp, C.c_size_t, vp]
     L.spec_verify_sample.argtypes = [C.POINTER(Batch), C.POINTER(Sampling), C.POINTER(Outputs),
@@ -118,7 +120,7 @@ def load_library(path: Optional[str] = None) -> C.CDLL:
                                         vp]
     L.spec_prefix_stats.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp]
     for f in ["spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_relaxed_topk",
-              "spec_verify_greedy_margin", "spec_verify_sample",
+              "spec_verify_greedy_margin", "spec_verify_greedy_active", "spec_verify_sample",
               "spec_draft_confidence", "spec_prefix_stats", "spec_abi_version"]:
         getattr(L, f).restype = C.c_int
     L.spec_step_state_bytes.restype = C.c_size_t
@@ -279,6 +281,25 @@ def verify_relaxed_topk(logits, cu_rows, draft_ids, relaxed_k, *, V: int, B: int
     o, res = _outputs(B, k_max, R_cap, logits.device, rows, stats)
     _check(L.spec_verify_relaxed_topk(C.byref(b), _dev(relaxed_k, "relaxed_k", torch.int32),
                                       C.byref(o), ws.data_ptr(), ws.numel(), _stream(stream)))
+    return res
+
+
+def verify_greedy_active(logits, cu_rows, draft_ids, vocab_ids, *, V: int, B: int, k_max: int,
+                         R_cap: Optional[int] = None, workspace=None, rows: bool = True,
+                         stats=None, stream=None) -> dict:
+    """spec_verify_greedy_active: greedy verification over V active columns,
+    column i standing for full token id vocab_ids[i]; drafts and outputs are
+    full ids."""
+    L = load_library()
+    R_cap = R_cap or B * (k_max + 1)
+    ws = workspace if workspace is not None else new_workspace(
+        R_cap, B, V, _logits_dtype(logits), logits.device)
+    if vocab_ids is None or vocab_ids.numel() < V:
+        raise SpecError("vocab_ids needs one full id per active column")
+    b = _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids)
+    o, res = _outputs(B, k_max, R_cap, logits.device, rows, stats)
+    _check(L.spec_verify_greedy_active(C.byref(b), _dev(vocab_ids, "vocab_ids", torch.int32),
+                                       C.byref(o), ws.data_ptr(), ws.numel(), _stream(stream)))
     return res
 
 

@@ -235,6 +235,21 @@ int spec_verify_relaxed_topk(const spec_batch *batch, const int32_t *relaxed_k,
     return run_verify(MODE_RELAXED, batch, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int spec_verify_greedy_active(const spec_batch *batch, const int32_t *vocab_ids,
+                              const spec_outputs *out, void *workspace, size_t workspace_bytes,
+                              spec_stream stream)
+{
+    int rc = check_batch(batch, out);
+    if (rc != SPEC_OK) return rc;
+    if (!vocab_ids) return SPEC_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < ws_bytes(batch->R_cap, batch->B, batch->V,
+                                                     static_cast<int>(elt_bytes(batch->dtype)), false))
+        return SPEC_ERR_WORKSPACE;
+    VerifyParams p = base_params(batch, out, workspace, false);
+    p.vocab_ids = vocab_ids;
+    return run_verify(MODE_GREEDY, batch, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int spec_verify_greedy_margin(const spec_batch *batch, const spec_margin *margin,
                               const spec_outputs *out, void *workspace, size_t workspace_bytes,
                               spec_stream stream)

@@ -41,6 +41,8 @@ struct VerifyParams {
     const int32_t *generated;
     const int32_t *protected_ids;
     int32_t n_protected, from_position, after_tokens;
+    // greedy over an active vocabulary: full token id of each column (or nullptr)
+    const int32_t *vocab_ids;
     // draft confidence (MODE_CONF: rows are draft positions)
     const int32_t *selected;
     float *conf;

@@ -1724,6 +1724,8 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
             p.conf[r] = cf;
             p.draft_token[r] = s;
         } else if (!queued) {
+            // active vocabulary: the argmax column's full token id
+            if (MODE == MODE_GREEDY && p.vocab_ids) y = __ldg(p.vocab_ids + AMAX);
             if (p.row_token) p.row_token[r] = y;
             p.ws_tok[r] = y;
             if (MODE == MODE_RELAXED || (MODE == MODE_GREEDY && p.margin)) p.ws_flag[r] = flag;

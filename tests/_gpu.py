@@ -44,6 +44,13 @@ def run_relaxed(sv, vb: W.VerifyBatch, K, **kw):
                                   k_max=vb.k_max, R_cap=vb.logits.shape[0], **kw)
 
 
+def run_active(sv, vb: W.VerifyBatch, draft_ids, vocab_ids, **kw):
+    return sv.verify_greedy_active(logits_tensor(vb.logits, vb.dtype), t(vb.cu_rows),
+                                   t(np.asarray(draft_ids, np.int32)),
+                                   t(np.asarray(vocab_ids, np.int32)), V=vb.V, B=vb.B,
+                                   k_max=vb.k_max, R_cap=vb.logits.shape[0], **kw)
+
+
 def run_margin(sv, vb: W.VerifyBatch, margin, generated=None, protected_ids=None, **kw):
     return sv.verify_greedy_margin(
         logits_tensor(vb.logits, vb.dtype), t(vb.cu_rows), t(vb.draft_ids),

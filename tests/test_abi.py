@@ -93,6 +93,8 @@ def test_host_argument_errors_launch_nothing(sv):
     s = Sampling(fake, None, fake, fake, fake, None, 0)
     assert L.spec_verify_sample(C.byref(b), C.byref(s), C.byref(outs), ws, n, None) == 1
     assert L.spec_verify_relaxed_topk(C.byref(b), None, C.byref(outs), ws, n, None) == 1
+    assert L.spec_verify_greedy_active(C.byref(b), None, C.byref(outs), ws, n, None) == 1
+    assert L.spec_verify_greedy_active(C.byref(b), fake, C.byref(outs), ws, n - 1, None) == 4
     from speculative_decoding_verification_ragged_gb300.binding import Margin
     for m, rc in [(Margin(None, None, None, 0, 0, 0), 1), (Margin(fake, None, None, -1, 0, 0), 1),
                   (Margin(fake, None, None, 3, 0, 0), 1)]:
