@@ -269,6 +269,34 @@ def verify_relaxed(logits, dtype, V, B, k_max, cu_rows, draft_ids, relaxed_k) ->
 
 
 # ----------------------------------------------------------------------------
+# Compact rows back to request slots
+# ----------------------------------------------------------------------------
+
+def restore_rows(compact: np.ndarray, cu_rows, B: int, k_max: int, out: np.ndarray):
+    """Restore of compact per-row outputs to request slots by device offsets
+    (xLLM "自适应投机推理" §"基于 MTP logits 的自适应 target 验证": compact
+    target outputs, e.g. hidden states, are restored by the device offsets
+    before the draft context is updated).  Row cu_rows[b] + j of `compact`
+    goes to slot b * (k_max + 1) + j of `out` for j = 0 .. k_b; other slots
+    are left as they are.  A request whose offsets are malformed (cu_rows[0]
+    != 0, a negative start, k_b outside [0, k_max], or rows beyond the
+    compact buffer) is skipped and reported.  Returns (out copy, status)."""
+    cu = _c(cu_rows, np.int64)
+    res = out.copy()
+    status = 0
+    R_cap = compact.shape[0]
+    for b in range(B):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        n = hi - lo
+        if cu[0] != 0 or lo < 0 or n < 1 or n - 1 > k_max or hi > R_cap:
+            status |= BAD_ROWS
+            continue
+        for j in range(n):
+            res[b * (k_max + 1) + j] = compact[lo + j]
+    return res, status
+
+
+# ----------------------------------------------------------------------------
 # Greedy verification over an active vocabulary
 # ----------------------------------------------------------------------------
 
