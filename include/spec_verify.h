@@ -318,6 +318,32 @@ SPEC_API int spec_draft_confidence(const spec_draft *draft, const spec_allocatio
 SPEC_API size_t spec_draft_workspace_bytes(int32_t B, int32_t k, int32_t V, int32_t dtype);
 
 /*
+ * Restore of compact rows to request slots (xLLM "自适应投机推理"
+ * §"基于 MTP logits 的自适应 target 验证": the outputs of the compact
+ * target rows, such as hidden states, are restored by the device offsets
+ * before the draft context is updated).  For each request b whose offsets
+ * are well formed (cu_rows as for the verify calls, and cu_rows[B] <= R_cap),
+ * slot b * (k_max + 1) + j of `out` receives the first row_bytes bytes of
+ * compact row cu_rows[b] + j, for j = 0 .. k_b.  Other slots are untouched.
+ * A malformed request is skipped and sets SPEC_STATUS_BAD_ROWS.
+ *   compact  device [R_cap rows, compact_ld bytes each], read only.
+ *   out      device [B * (k_max + 1) rows, out_ld bytes each]; must not
+ *            overlap `compact`.
+ *   cu_rows  device [B + 1], e.g. spec_draft_confidence's output.
+ *   status   device [1] or NULL.
+ * Rows are opaque bytes, so any element type works.  Returns
+ * SPEC_ERR_INVALID_ARG for NULL pointers, B < 1, R_cap < 1, k_max < 0,
+ * row_bytes < 1 or a stride below row_bytes; SPEC_ERR_UNSUPPORTED for
+ * k_max > 31, row_bytes > 2^30, B * (k_max + 1) > 2^31 - 1, or when
+ * row_bytes, either stride or either base address is not a multiple of 16.
+ * One kernel launch; HBM-bound (each restored row read and written once).
+ */
+SPEC_API int spec_restore_rows(const void *compact, int64_t compact_ld, int32_t R_cap,
+                               const int32_t *cu_rows, int32_t B, int32_t k_max,
+                               int64_t row_bytes, void *out, int64_t out_ld, uint32_t *status,
+                               spec_stream stream);
+
+/*
  * A8 (xLLM "自适应投机推理" §"自适应 draft 步长（MTP）"): accumulate
  * acc[j] += #{b : a_b > j}, ver[j] += #{b : k_b > j} for j < k_max and
  * hist[a_b] += 1 (hist may be NULL).  prefix_acceptance[j] = acc[j] / ver[j].

@@ -7,7 +7,7 @@ in-tree build (_build.py) and a thin ctypes binding (binding.py).
 from ._build import build  # noqa: F401
 from .binding import (  # noqa: F401
     EXPORTS, SpecError, StepController, draft_confidence, load_library, new_workspace,
-    prefix_stats, step_cost_additive, step_cost_sps,
+    prefix_stats, restore_rows, step_cost_additive, step_cost_sps,
     verify_greedy, verify_greedy_active, verify_greedy_margin, verify_greedy_noalloc, verify_relaxed_topk,
     verify_sample, workspace_bytes,
 )
@@ -15,4 +15,4 @@ from .binding import (  # noqa: F401
 __all__ = ["build", "load_library", "new_workspace", "workspace_bytes", "verify_greedy",
            "verify_greedy_noalloc", "verify_greedy_margin", "verify_greedy_active",
            "verify_relaxed_topk", "verify_sample", "draft_confidence", "prefix_stats",
-           "StepController", "step_cost_sps", "step_cost_additive", "SpecError", "EXPORTS"]
+           "restore_rows", "StepController", "step_cost_sps", "step_cost_additive", "SpecError", "EXPORTS"]

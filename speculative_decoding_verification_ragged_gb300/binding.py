@@ -35,7 +35,8 @@ STATUS_BAD_MARGIN = 0x200
 
 EXPORTS = ["spec_workspace_bytes", "spec_draft_workspace_bytes", "spec_verify_greedy",
            "spec_verify_greedy_noalloc", "spec_verify_relaxed_topk",
-           "spec_verify_greedy_margin", "spec_verify_greedy_active", "spec_verify_sample", "spec_draft_confidence", "spec_prefix_stats",
+           "spec_verify_greedy_margin", "spec_verify_greedy_active", "spec_verify_sample",
+           "spec_draft_confidence", "spec_prefix_stats", "spec_restore_rows",
            "spec_result_string", "spec_last_cuda_error", "spec_abi_version",
            "spec_step_state_bytes", "spec_step_init", "spec_step_update", "spec_step_query",
            "spec_step_cost_sps", "spec_step_cost_additive"]
@@ -119,6 +120,8 @@ def load_library(path: Optional[str] = None) -> C.CDLL:
     L.spec_draft_confidence.argtypes = [C.POINTER(Draft), C.POINTER(Allocation), vp, C.c_size_t,
                                         vp]
     L.spec_prefix_stats.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp]
+    L.spec_restore_rows.argtypes = [vp, i64, i32, vp, i32, i32, i64, vp, i64, vp, vp]
+    L.spec_restore_rows.restype = C.c_int
     for f in ["spec_verify_greedy", "spec_verify_greedy_noalloc", "spec_verify_relaxed_topk",
               "spec_verify_greedy_margin", "spec_verify_greedy_active", "spec_verify_sample",
               "spec_draft_confidence", "spec_prefix_stats", "spec_abi_version"]:
@@ -382,6 +385,30 @@ def draft_confidence(draft_logits, *, V: int, B: int, k: int, selected=None,
     _check(L.spec_draft_confidence(C.byref(d), C.byref(a), ws.data_ptr(), ws.numel(),
                                    _stream(stream)))
     return res
+
+
+def restore_rows(compact: torch.Tensor, cu_rows, out: torch.Tensor, *, B: int, k_max: int,
+                 status=None, stream=None) -> torch.Tensor:
+    """spec_restore_rows: compact row cu_rows[b] + j goes to row
+    b * (k_max + 1) + j of `out` for j <= k_b; other rows of `out` are left
+    as they are.  compact [R_cap, H] and out [B * (k_max + 1), H] are 2-D
+    device tensors of one dtype whose rows are 16-byte multiples."""
+    L = load_library()
+    if compact.dim() != 2 or out.dim() != 2 or compact.dtype != out.dtype:
+        raise SpecError("compact and out must be 2-D tensors of one dtype")
+    if compact.shape[1] != out.shape[1] or out.shape[0] < B * (k_max + 1):
+        raise SpecError("out needs B * (k_max + 1) rows of the compact row width")
+    if compact.stride(1) != 1 or out.stride(1) != 1:
+        raise SpecError("rows must be contiguous")
+    for x, what in [(compact, "compact"), (out, "out")]:
+        if not x.is_cuda:
+            raise SpecError("%s must be a CUDA tensor" % what)
+    es = compact.element_size()
+    _check(L.spec_restore_rows(compact.data_ptr(), compact.stride(0) * es, compact.shape[0],
+                               _dev(cu_rows, "cu_rows", torch.int32), B, k_max,
+                               compact.shape[1] * es, out.data_ptr(), out.stride(0) * es,
+                               _dev(status, "status", torch.int32), _stream(stream)))
+    return out
 
 
 def prefix_stats(accepted_len, cu_rows, acc, ver, hist=None, status=None, *, B: int, k_max: int,

@@ -373,6 +373,25 @@ int spec_prefix_stats(const int32_t *accepted_len, const int32_t *cu_rows, int32
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 
+int spec_restore_rows(const void *compact, int64_t compact_ld, int32_t R_cap,
+                      const int32_t *cu_rows, int32_t B, int32_t k_max, int64_t row_bytes,
+                      void *out, int64_t out_ld, uint32_t *status, spec_stream stream)
+{
+    if (!compact || !cu_rows || !out) return SPEC_ERR_INVALID_ARG;
+    if (B < 1 || R_cap < 1 || k_max < 0 || row_bytes < 1 || compact_ld < row_bytes ||
+        out_ld < row_bytes)
+        return SPEC_ERR_INVALID_ARG;
+    if (k_max > 31 || row_bytes > (static_cast<int64_t>(1) << 30)) return SPEC_ERR_UNSUPPORTED;
+    if (row_bytes % 16 || compact_ld % 16 || out_ld % 16 ||
+        reinterpret_cast<uintptr_t>(compact) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+        return SPEC_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(B) * (k_max + 1) > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
+    const cudaError_t e = launch_restore_rows(compact, compact_ld, R_cap, cu_rows, B, k_max,
+                                              row_bytes, out, out_ld, status,
+                                              reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+}
+
 const char *spec_result_string(int code)
 {
     switch (code) {

@@ -174,6 +174,64 @@ cudaError_t launch_alloc(const AllocParams &p, cudaStream_t stream)
     return cudaGetLastError();
 }
 
+// ------------------------------------------ compact rows to request slots --
+
+// xLLM "自适应投机推理" §"基于 MTP logits 的自适应 target 验证": outputs of the
+// compact target rows (hidden states, per-row results) are restored to their
+// request slots by the device offsets.  Slot s = (b, j) takes compact row
+// cu_rows[b] + j when j <= k_b; other slots are left untouched.  Rows are
+// opaque bytes in 16-byte vectors (alignment checked on the host).
+// blockIdx.x selects an 8 KiB piece of the row and blockIdx.y strides over
+// the slots; a thread moves two vectors, both loads issued before the
+// stores.  HBM-bound: each restored row is read once and written once.
+constexpr int kRestoreThreads = 256;
+constexpr int kRestoreVecs = 2 * kRestoreThreads;
+
+__global__ void __launch_bounds__(kRestoreThreads) restore_rows_kernel(
+    const uint8_t *__restrict__ src, int64_t src_ld, int32_t R_cap,
+    const int32_t *__restrict__ cu_rows, int32_t B, int32_t k_max, int64_t vecs,
+    uint8_t *__restrict__ dst, int64_t dst_ld, uint32_t *status)
+{
+    const int32_t k1 = k_max + 1;
+    const int32_t slots = B * k1;
+    const int32_t c0 = __ldg(cu_rows);
+    const int64_t va = static_cast<int64_t>(blockIdx.x) * kRestoreVecs + threadIdx.x;
+    const int64_t vb = va + kRestoreThreads;
+    for (int32_t s = blockIdx.y; s < slots; s += gridDim.y) {
+        const int32_t b = s / k1, j = s - b * k1;
+        const int64_t lo = __ldg(cu_rows + b), hi = __ldg(cu_rows + b + 1);
+        const int64_t n = hi - lo;
+        const bool ok = c0 == 0 && lo >= 0 && n >= 1 && n - 1 <= k_max && hi <= R_cap;
+        if (!ok) {
+            if (j == 0 && blockIdx.x == 0 && threadIdx.x == 0) set_status(status, SPEC_STATUS_BAD_ROWS);
+            continue;
+        }
+        if (j >= n) continue;
+        const uint4 *in = reinterpret_cast<const uint4 *>(src + (lo + j) * src_ld);
+        uint4 *out = reinterpret_cast<uint4 *>(dst + static_cast<int64_t>(s) * dst_ld);
+        uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;
+        if (va < vecs) xa = __ldcs(in + va);
+        if (vb < vecs) xb = __ldcs(in + vb);
+        if (va < vecs) __stcs(out + va, xa);
+        if (vb < vecs) __stcs(out + vb, xb);
+    }
+}
+
+cudaError_t launch_restore_rows(const void *src, int64_t src_ld, int32_t R_cap,
+                                const int32_t *cu_rows, int32_t B, int32_t k_max,
+                                int64_t row_bytes, void *dst, int64_t dst_ld, uint32_t *status,
+                                cudaStream_t stream)
+{
+    const int64_t vecs = row_bytes / 16;
+    const int64_t slots = static_cast<int64_t>(B) * (k_max + 1);
+    const dim3 grid(static_cast<unsigned>((vecs + kRestoreVecs - 1) / kRestoreVecs),
+                    static_cast<unsigned>(slots < 65535 ? slots : 65535));
+    restore_rows_kernel<<<grid, kRestoreThreads, 0, stream>>>(
+        static_cast<const uint8_t *>(src), src_ld, R_cap, cu_rows, B, k_max, vecs,
+        static_cast<uint8_t *>(dst), dst_ld, status);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------- prefix statistics -----
 
 __global__ void __launch_bounds__(1024) prefix_stats_kernel(const int32_t *accepted_len,

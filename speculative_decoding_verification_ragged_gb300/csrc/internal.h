@@ -93,6 +93,10 @@ struct AllocParams {
 // Host launchers (return cudaError_t of the launch).
 cudaError_t launch_verify(int mode, int dtype, const VerifyParams &p, cudaStream_t stream);
 cudaError_t launch_alloc(const AllocParams &p, cudaStream_t stream);
+cudaError_t launch_restore_rows(const void *src, int64_t src_ld, int32_t R_cap,
+                                const int32_t *cu_rows, int32_t B, int32_t k_max,
+                                int64_t row_bytes, void *dst, int64_t dst_ld, uint32_t *status,
+                                cudaStream_t stream);
 cudaError_t launch_prefix_stats(const int32_t *accepted_len, const int32_t *cu_rows, int32_t B,
                                 int32_t k_max, int64_t *acc, int64_t *ver, int64_t *hist,
                                 uint32_t *status, cudaStream_t stream);

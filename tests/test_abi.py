@@ -103,5 +103,15 @@ def test_host_argument_errors_launch_nothing(sv):
     assert L.spec_verify_greedy_margin(C.byref(b), C.byref(m), C.byref(outs), ws, n - 1, None) == 4
     assert L.spec_verify_greedy_margin(C.byref(b), None, C.byref(outs), ws, n, None) == 1
     assert L.spec_prefix_stats(fake, fake, 4, 40, fake, fake, None, None, None) == 2
+    # restore: every case below fails its host checks, so nothing launches
+    rr, big = L.spec_restore_rows, C.c_void_p(0x10000)
+    assert rr(None, 64, 8, fake, 2, 3, 64, big, 64, None, None) == 1
+    assert rr(big, 64, 8, fake, 0, 3, 64, big, 64, None, None) == 1
+    assert rr(big, 32, 8, fake, 2, 3, 64, big, 64, None, None) == 1      # stride < row
+    assert rr(big, 64, 8, fake, 2, 32, 64, big, 64, None, None) == 2     # k_max > 31
+    assert rr(big, 64, 8, fake, 2, 3, 56, big, 64, None, None) == 2      # row not 16-byte
+    assert rr(big, 72, 8, fake, 2, 3, 64, big, 72, None, None) == 2      # stride not 16-byte
+    assert rr(C.c_void_p(0x10008), 64, 8, fake, 2, 3, 64, big, 64, None, None) == 2
+    assert rr(big, 64, 8, fake, 1 << 28, 31, 64, big, 64, None, None) == 2   # too many slots
     assert L.spec_prefix_stats(fake, fake, 0, 4, fake, fake, None, None, None) == 1
     assert L.spec_result_string(4) == b"SPEC_ERR_WORKSPACE"
