@@ -258,7 +258,16 @@ def run_ours(args) -> None:
     # job-wide prefix-acceptance counters (one sum all-reduce, at read time)
     shard.reduce_prefix_stats(acc, ver, hist)
 
+    prefix_acc = [round(float(x), 4) for x in
+                  shard.prefix_acceptance(acc.cpu().numpy(), ver.cpu().numpy())]
     entries = time_entry_points(sv, dev, stream, args) if (rank == 0 and not args.no_entries) else None
+    entry_errors = None
+    if entries is not None:
+        # the later entry points run last and cannot cost the line above
+        try:
+            entries.update(time_more_entry_points(sv, dev, stream, args))
+        except Exception as exc:  # noqa: BLE001 -- reported in the JSON line
+            entry_errors = "%s: %s" % (type(exc).__name__, exc)
 
     if rank == 0:
         peaks = measured_peaks()
@@ -298,14 +307,15 @@ def run_ours(args) -> None:
             "e2e": {"value": round(world * R * e2e_steps / (e2e_ms * 1e-3), 1), "unit": "rows/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": LAUNCHES_PER_CALL * args.steps,
-            "prefix_acceptance": [round(float(x), 4) for x in
-                                  shard.prefix_acceptance(acc.cpu().numpy(), ver.cpu().numpy())],
+            "prefix_acceptance": prefix_acc,
             "clocks": clocks.summary(),
         }
         if entries is not None:
             for e in entries.values():
                 e["pct_of_peak"] = round(100 * e["hbm_gbs"] / peaks["hbm_gbs"], 1)
             line["entry_points"] = entries
+            if entry_errors:
+                line["entry_point_errors"] = entry_errors
             line["step_controller"] = time_step_controller(sv)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(vb, p)
@@ -439,6 +449,66 @@ def time_entry_points(sv, dev, stream, args) -> dict:
                                hist.data_ptr(), None, s))
     ms = _time_launches(stats, n, stream)
     out["spec_prefix_stats"] = {"workload": "B=128 k=4", "us": round(ms * 1e3, 2), "hbm_gbs": 0.0}
+    return out
+
+
+def time_more_entry_points(sv, dev, stream, args) -> dict:
+    """Device time of greedy verification over an active vocabulary and of
+    the compact-row restore (inputs rotate over copies larger than L2)."""
+    import ctypes as C
+    import torch
+    from speculative_decoding_verification_ragged_gb300 import binding as Bd
+
+    L = Bd.load_library()
+    s = stream.cuda_stream
+    n = args.entry_launches
+    out = {}
+
+    def ok(rc):
+        if rc:
+            raise RuntimeError("entry point returned %d" % rc)
+
+    g = torch.Generator(device=dev).manual_seed(21)
+    # greedy over 32000 active columns of a 152064-token vocabulary
+    B, K, Va, Vfull = 128, 4, 32_000, 152_064
+    R = B * (K + 1)
+    sets = [(3 * torch.randn(R, Va, device=dev, generator=g)).to(torch.bfloat16)
+            for _ in range(4)]
+    ids = torch.randperm(Vfull, device=dev, generator=g)[:Va].sort().values.to(torch.int32)
+    cu = torch.arange(0, R + 1, K + 1, dtype=torch.int32, device=dev)
+    dr = ids[torch.randint(0, Va, (R,), device=dev, generator=g)].contiguous()
+    ws = sv.new_workspace(R, B, Va, torch.bfloat16, dev)
+    b = Bd._batch(sets[0], Va, B, K, R, cu, dr)
+    o, _ = Bd._outputs(B, K, R, dev, True, None)
+
+    def active(i):
+        b.logits = sets[i % len(sets)].data_ptr()
+        ok(L.spec_verify_greedy_active(C.byref(b), ids.data_ptr(), C.byref(o), ws.data_ptr(),
+                                       ws.numel(), s))
+    for i in range(5):
+        active(i)
+    ms = _time_launches(active, n, stream)
+    out["spec_verify_greedy_active"] = {
+        "workload": "B=128 k=4, 32000 active columns of 152064, bf16 N(0,3), row outputs",
+        "rows": R, "us": round(ms * 1e3, 2), "hbm_gbs": round(R * Va * 2 / (ms * 1e-3) / 1e9, 1)}
+    del sets
+    # hidden states of the compact rows back to their slots: B=128, k=4,
+    # H=5120 bf16 (10 KiB rows), every request keeping all its rows
+    H = 5120
+    # (12 source/destination pairs of 6.6 MB each rotate through more than L2)
+    comp = [torch.randn(R, H, device=dev, generator=g).to(torch.bfloat16) for _ in range(12)]
+    dst = [torch.empty(R, H, device=dev, dtype=torch.bfloat16) for _ in range(12)]
+
+    def restore(i):
+        c, d = comp[i % 12], dst[i % 12]
+        ok(L.spec_restore_rows(c.data_ptr(), H * 2, R, cu.data_ptr(), B, K, H * 2, d.data_ptr(),
+                               H * 2, None, s))
+    for i in range(5):
+        restore(i)
+    ms = _time_launches(restore, n, stream)
+    out["spec_restore_rows"] = {
+        "workload": "B=128 k=4 rows of 5120 bf16, every slot restored",
+        "rows": R, "us": round(ms * 1e3, 2), "hbm_gbs": round(2 * R * H * 2 / (ms * 1e-3) / 1e9, 1)}
     return out
 
 
