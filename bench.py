@@ -21,6 +21,7 @@ import hashlib
 import re
 import json
 import os
+import platform
 import statistics
 import sys
 import threading
@@ -303,7 +304,10 @@ def run_ours(args) -> None:
                          "kernel": "spec_verify_sample call (row_info + stream_chunks + "
                                    "finish_rows + heavy_rows kernels, bf16)",
                          "algorithmic_bytes_per_launch": bytes_per_launch,
-                         "mean_launch_us": round(mean_launch_ms * 1e3, 3)},
+                         "mean_launch_us": round(mean_launch_ms * 1e3, 3),
+                         "launch_us_p10_median_p90": [
+                             round(float(np.percentile(launch_ms, q)) * 1e3, 3)
+                             for q in (10, 50, 90)]},
             "e2e": {"value": round(world * R * e2e_steps / (e2e_ms * 1e-3), 1), "unit": "rows/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": LAUNCHES_PER_CALL * args.steps,
@@ -558,9 +562,40 @@ def cpu_baseline(vb, p, budget_s: float = 10.0) -> dict:
         if time.perf_counter() - t0 > budget_s or n >= 20:
             break
     dt = time.perf_counter() - t0
+    # one thread, on the first 16 requests of the same batch
+    nb = min(16, vb.B)
+    r1 = int(vb.cu_rows[nb])
+    sub = W.VerifyBatch(vb.logits[:r1], vb.dtype, vb.V, nb, vb.k_max, vb.cu_rows[:nb + 1],
+                        vb.draft_ids[:r1])
+    ps = W.SampleParams(p.temperature[:nb], p.top_k[:nb], p.top_p[:nb], p.min_p[:nb],
+                        p.seed[:nb], p.request_id[:nb], p.step)
+    oracle.threads(1)
+    t1 = time.perf_counter()
+    oracle.verify_sample(sub.logits, sub.dtype, sub.V, sub.B, sub.k_max, sub.cu_rows,
+                         sub.draft_ids, ps)
+    dt1 = time.perf_counter() - t1
+    oracle.threads(cores)
     return {"value": round(rows / dt, 2), "unit": "rows/s", "cores": cores, "kind": "oracle",
             "sample": "%d full batch(es) of the benchmark workload (%d rows each), fp64 C oracle "
-                      "with OpenMP over rows" % (n, vb.R)}
+                      "with OpenMP over rows" % (n, vb.R),
+            "single_thread": {"value": round(r1 / dt1, 2), "unit": "rows/s",
+                              "sample": "the first %d requests (%d rows) of one batch, one thread"
+                                        % (nb, r1)},
+            "cpu_model": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (x86 and Arm /proc/cpuinfo layouts)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model Name", "Hardware", "CPU part"):
+        m = re.search(r"^%s\s*:\s*(.+)$" % key, info, re.M)
+        if m:
+            return "%s (%s)" % (m.group(1).strip(), platform.machine())
+    return platform.machine()
 
 
 # ------------------------------------------------------ reference arm -----
