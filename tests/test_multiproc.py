@@ -2,7 +2,9 @@
 request sharding with rebased cu_rows needs no exchange for verification
 (each shard's results equal the whole batch's), and one sum all-reduce of the
 prefix-acceptance counters gives the job-wide counters; the bench's job time
-is the slowest rank's.  The oracle stands in for the GPU path on each rank."""
+is the slowest rank's.  The oracle stands in for the GPU path on each rank.
+The adaptive step controller, fed the job-wide counters on every rank, takes
+the same batch-uniform step everywhere without exchanging its decision."""
 import os
 import socket
 import tempfile
@@ -93,3 +95,53 @@ def test_two_gloo_ranks_shard_requests_and_reduce_counters():
         # the job's time is its slowest rank's; units add up over ranks
         assert r["slow"][0] == 2.0
         assert r["rows"][0] == vb.R
+
+
+def _ctl_rank_main(rank, world, port, out_dir):
+    import torch
+    import torch.distributed as dist
+    import speculative_decoding_verification_ragged_gb300 as sv
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    rng = np.random.default_rng(100 + rank)           # each rank its own requests
+    K = 5
+    ctl = sv.StepController(1, K, 3)
+    k, ks, accs, vers, bs = 3, [], [], [], []
+    for t in range(40):
+        B_local = 12 + 5 * rank
+        alpha = 0.9 if t < 20 else 0.3                # the acceptance collapses halfway
+        a = np.minimum(rng.geometric(1 - alpha, size=B_local) - 1, k)
+        acc = torch.tensor([(a > j).sum() for j in range(K)], dtype=torch.int64)
+        ver = torch.tensor([B_local if j < k else 0 for j in range(K)], dtype=torch.int64)
+        shard.reduce_prefix_stats(acc, ver)           # job-wide counters on every rank
+        B = int(shard.sum_over_ranks(float(B_local)))
+        cost = sv.step_cost_sps(B, K, [64, 128, 192, 256], [90.0, 70.0, 55.0, 45.0])
+        k = sv.StepController.update(ctl, acc.numpy(), ver.numpy(), cost, B)
+        ks.append(k); accs.append(acc.numpy()); vers.append(ver.numpy()); bs.append(B)
+    np.savez(os.path.join(out_dir, "ctl%d.npz" % rank), ks=np.array(ks), acc=np.array(accs),
+             ver=np.array(vers), B=np.array(bs))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_same_adaptive_step():
+    import torch.multiprocessing as mp
+    import speculative_decoding_verification_ragged_gb300 as sv
+    from oracle.step_policy import StepController, step_cost_sps
+    sv.build()
+    world = 2
+    with tempfile.TemporaryDirectory() as d:
+        mp.start_processes(_ctl_rank_main, args=(world, _free_port(), d), nprocs=world,
+                           start_method="spawn", join=True)
+        res = [np.load(os.path.join(d, "ctl%d.npz" % r)) for r in range(world)]
+    np.testing.assert_array_equal(res[0]["ks"], res[1]["ks"])
+    np.testing.assert_array_equal(res[0]["acc"], res[1]["acc"])
+    # the oracle controller on the job-wide counters takes the same steps
+    orc = StepController(1, 5, 3)
+    ks = [orc.update(a, v, step_cost_sps(int(B), 5, [64, 128, 192, 256],
+                                         [90.0, 70.0, 55.0, 45.0]), int(B))
+          for a, v, B in zip(res[0]["acc"], res[0]["ver"], res[0]["B"])]
+    np.testing.assert_array_equal(res[0]["ks"], np.array(ks))
+    # high acceptance lengthens the step, the collapse shortens it again
+    assert ks[3] == 3 and ks[19] == 5 and ks[-1] < 5
