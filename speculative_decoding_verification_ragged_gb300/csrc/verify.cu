@@ -1,13 +1,16 @@
 // verify.cu -- kernels for ragged packed logits: fused max / LSE / argmax,
-// greedy and relaxed top-K acceptance, the filtered Gumbel-max sampler with
-// the point-mass rejection chain, and the draft confidence.
+// greedy acceptance (strict, loosened by a confidence margin, or over an
+// active vocabulary), relaxed top-K acceptance, the filtered Gumbel-max
+// sampler with the point-mass rejection chain, and the draft confidence.
 //
 // Kernels per call, chained with programmatic dependent launch:
 //
 //   prologue, one warp per packed row: the owner request (32-way search of
 //     cu_rows), the row's position and validity and the owner's parameters,
 //     as a 64-byte row record; requests without a valid row range get their
-//     outputs here.
+//     outputs here.  With a confidence margin it also decides whether the
+//     margin applies to the row (position, generated-token count, a warp
+//     scan of the protected ids) and records the draft's logit (NaN if not).
 //   stream, one CTA per (row, chunk of kChunkBytes) on a two-dimensional
 //     grid (the sampler chunk-major, the other modes row-major): thread 0
 //     issues one 1-D TMA bulk copy of the chunk's 16-byte-aligned body into
@@ -38,7 +41,9 @@
 //   finish, one CTA per row: combine the chunk summaries, then for the
 //     sampler run radix selects (exact k-th largest value, exact top-p mass
 //     crossing) over the candidate lists staged in shared memory and
-//     Gumbel-max over the survivors with Philox4x32-10 uniforms; bf16
+//     Gumbel-max over the survivors with Philox4x32-10 uniforms (greedy
+//     rows: the argmax, mapped to its full id over an active vocabulary;
+//     with a margin, a per-row flag from the gap max - z[d]); bf16
 //     survivors spanning at most kTally values take top-p over per-value
 //     tallies instead.  Pure top-p brackets the nucleus boundary with the
 //     combined bins; when the lists cover the undecided band the row is
@@ -61,7 +66,9 @@
 // temperature 0 = greedy, ordinary top-k/top-p/min-p semantics),
 // §"基于 MTP logits 的自适应 target 验证" (exp(selected - logsumexp)),
 // "vllm-hust-vSpec" README §"EAGLE 功能" (strict top-1 and relaxed top-K
-// acceptance with a strict prefix, no per-request host sync).
+// acceptance with a strict prefix, no per-request host sync, the active
+// vocabulary with a full token-id map), §"启动" and §"通用参数" (the
+// confidence margin and its position, token-count and protected-id options).
 #include <cfloat>
 #include <climits>
 #include <cmath>
