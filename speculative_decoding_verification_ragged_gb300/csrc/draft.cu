@@ -1,8 +1,9 @@
-// draft.cu -- prefix-budget allocation / packing and prefix-acceptance
-// counters (xLLM docs "自适应投机推理": §"基于 MTP logits 的自适应 target
-// 验证" -- confidence kept on device, prefix allocation and packing with
-// device offsets; §"自适应 draft 步长（MTP）" -- per-position prefix
-// acceptance).  The draft confidences themselves come from the row kernel
+// draft.cu -- prefix-budget allocation / packing, the restore of compact
+// rows to request slots, and prefix-acceptance counters (xLLM docs
+// "自适应投机推理": §"基于 MTP logits 的自适应 target 验证" -- confidence kept
+// on device, prefix allocation and packing with device offsets, compact
+// target outputs restored by those offsets; §"自适应 draft 步长（MTP）" --
+// per-position prefix acceptance).  The draft confidences themselves come from the row kernel
 // in verify.cu (MODE_CONF).
 #include <climits>
 
