@@ -14,12 +14,19 @@
  *       is greedy, and top-k / top-p / min-p follow the ordinary sampler.
  *       §"基于 MTP logits 的自适应 target 验证": the draft confidence
  *       exp(selected_logit - logsumexp(draft_logits)), kept on the device for
- *       prefix allocation and packing with device offsets.
+ *       prefix allocation and packing with device offsets, and the restore
+ *       of the compact target rows' outputs by those offsets.
  *       §"自适应 draft 步长（MTP）": per-position prefix acceptance feeding the
  *       controller objective B * (1 + sum(prefix_acceptance[:k])) / cost_ms.
  *   - "vllm-hust-vSpec" README, §"EAGLE 功能" and §"支持范围": strict greedy
  *       top-1 acceptance, and relaxed top-K acceptance with a strict prefix;
- *       acceptance without a per-request device-to-host sync.
+ *       acceptance without a per-request device-to-host sync; the active
+ *       vocabulary with a full token-id map (also §"代码所有权").
+ *       §"启动" and §"通用参数": greedy acceptance loosened by a confidence
+ *       margin, from a position or after a token count, never for protected
+ *       token ids.
+ *   The host-side adaptive step controller that consumes the counters is
+ *   declared in spec_step.h.
  *
  * Conventions (all entry points):
  *   - Every pointer argument is DEVICE memory owned by the caller unless the
