@@ -6,8 +6,9 @@ inputs and outputs.
 
 The GPU test compares it with spec_verify_greedy, which takes a caller-owned
 workspace, on two calls in a row with different batches (the shared scratch
-keeps the previous call's contents).  This file is collected last so that a
-run stopping at the first failure has run every other test before it."""
+keeps the previous call's contents).  This file is collected after the
+other GPU files, so that a run stopping at the first failure has run them
+first."""
 import ctypes as C
 
 import numpy as np

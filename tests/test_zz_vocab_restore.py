@@ -1,6 +1,8 @@
 """GPU parity (through the C ABI) of greedy verification over an active
 vocabulary and of the restore of compact rows to request slots, against the
-CPU oracle.  Bit-exact."""
+CPU oracle.  Bit-exact.  This file is collected last: its paths are the
+newest, so a run stopping at the first failure has run every other test
+before it."""
 import numpy as np
 import pytest
 
