@@ -115,3 +115,27 @@ def test_host_argument_errors_launch_nothing(sv):
     assert rr(big, 64, 8, fake, 1 << 28, 31, 64, big, 64, None, None) == 2   # too many slots
     assert L.spec_prefix_stats(fake, fake, 0, 4, fake, fake, None, None, None) == 1
     assert L.spec_result_string(4) == b"SPEC_ERR_WORKSPACE"
+
+
+def test_binding_rejects_bad_tensors_before_any_call(sv):
+    """The Python binding checks devices, dtypes and shapes of the new entry
+    points' tensors before calling the library (CPU tensors never reach it)."""
+    import torch
+    from speculative_decoding_verification_ragged_gb300 import SpecError
+    x = torch.zeros(10, 8)
+    cu = torch.tensor([0, 5, 10], dtype=torch.int32)
+    d = torch.zeros(10, dtype=torch.int32)
+    with pytest.raises(SpecError):
+        sv.verify_greedy_margin(x, cu, d, torch.zeros(2), V=8, B=2, k_max=4,
+                                workspace=torch.zeros(1, dtype=torch.uint8))
+    with pytest.raises(SpecError):                    # map shorter than the active columns
+        sv.verify_greedy_active(x, cu, d, torch.zeros(7, dtype=torch.int32), V=8, B=2, k_max=4,
+                                workspace=torch.zeros(1, dtype=torch.uint8))
+    with pytest.raises(SpecError):                    # one dtype for both buffers
+        sv.restore_rows(torch.zeros(4, 8), cu, torch.zeros(8, 8, dtype=torch.float64), B=2, k_max=3)
+    with pytest.raises(SpecError):                    # out too short for B * (k_max + 1) slots
+        sv.restore_rows(torch.zeros(4, 8), cu, torch.zeros(7, 8), B=2, k_max=3)
+    with pytest.raises(SpecError):                    # row widths differ
+        sv.restore_rows(torch.zeros(4, 8), cu, torch.zeros(8, 4), B=2, k_max=3)
+    with pytest.raises(SpecError):                    # host tensors
+        sv.restore_rows(torch.zeros(4, 8), cu, torch.zeros(8, 8), B=2, k_max=3)
