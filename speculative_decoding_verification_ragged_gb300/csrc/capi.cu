@@ -30,20 +30,18 @@ struct WsLayout {
     int32_t *tok, *flag;
     uint32_t *ticket, *rticket;
     void *info, *part, *cand;
-    float *bins;
-    int32_t *hrows;
+    int4 *queue;
 };
 
 // tok [R_cap] | flag [R_cap] | ticket [B] | rticket [R_cap] | info [R_cap * 64 B] |
-// part [R_cap * nchunk * 32 B] | bins, cand, hrows (sampler only); 256-byte aligned
+// part [R_cap * nchunk * 32 B] | cand, queue (sampler only); 256-byte aligned
 size_t ws_bytes(int32_t R_cap, int32_t B, int32_t V, int elt, bool sampling)
 {
     const size_t R = static_cast<size_t>(R_cap);
     const size_t rc = R * static_cast<size_t>(chunks_per_row(V, elt));
     size_t n = 3 * align256(R * 4) + align256(static_cast<size_t>(B) * 4) + align256(R * 64) +
                align256(rc * 32);
-    if (sampling)
-        n += align256(rc * kWsBins * 4) + align256(rc * kWsCandCap * 8) + align256((R + 1) * 4);
+    if (sampling) n += align256(rc * kWsCandCap * 8) + align256((R + 1) * 16);
     return n;
 }
 
@@ -66,11 +64,9 @@ WsLayout ws_layout(void *ws, int32_t R_cap, int32_t B, int32_t V, int elt, bool 
     l.part = p;
     p += align256(rc * 32);
     if (sampling) {
-        l.bins = reinterpret_cast<float *>(p);
-        p += align256(rc * kWsBins * 4);
         l.cand = p;
         p += align256(rc * kWsCandCap * 8);
-        l.hrows = reinterpret_cast<int32_t *>(p);
+        l.queue = reinterpret_cast<int4 *>(p);
     }
     return l;
 }
@@ -127,9 +123,8 @@ VerifyParams base_params(const spec_batch *b, const spec_outputs *o, void *ws, b
     p.ws_rticket = l.rticket;
     p.ws_info = l.info;
     p.ws_part = l.part;
-    p.ws_bins = l.bins;
     p.ws_cand = l.cand;
-    p.ws_hrows = l.hrows;
+    p.ws_queue = l.queue;
     p.nchunk = chunks_per_row(b->V, elt);
     p.n_rows = b->R_cap;
     return p;

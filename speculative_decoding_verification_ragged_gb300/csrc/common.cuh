@@ -113,6 +113,27 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Barrier of the CTA's compute warps only (named barrier 2, kThreads
+// threads): the ticket warp of the row kernel never joins it.
+__device__ __forceinline__ void csync()
+{
+    asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");
+}
+
+// csync() that also counts the threads whose predicate is true
+__device__ __forceinline__ int csync_count(bool pred)
+{
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.popc.u32 %0, 2, %2, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "n"(kThreads)
+        : "memory");
+    return r;
+}
+
 // Release / acquire fence at GPU scope (orders this CTA's earlier writes,
 // made visible to this thread by a CTA barrier, before a following atomic;
 // or a preceding atomic before later reads).

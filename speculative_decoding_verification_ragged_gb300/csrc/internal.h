@@ -10,14 +10,15 @@ namespace specv {
 enum Mode : int { MODE_GREEDY = 0, MODE_RELAXED = 1, MODE_SAMPLE = 2, MODE_CONF = 3 };
 
 // Workspace of the row kernel, per packed row r and chunk c (a row is split
-// into nchunk = ceil(V * elt / kChunkBytes) chunks, one CTA each):
+// into nchunk = ceil(V * elt / kChunkBytes) chunks, one work item each):
 //   info[r]     (64 bytes) owner request and parameters of the row
 //   part[r][c]  (32 bytes) chunk reduction and sampler summary
-//   bins[r][c]  (kWsBins floats) pure top-p mass bins         (sampler only)
-//   cand[r][c]  (kWsCandCap (value, index) pairs) candidates  (sampler only)
-//   hrows       (1 + R_cap int32) rows queued for a second pass (sampler only)
+//   cand[r][c]  (kWsCandCap (value, index) pairs) candidate lists, or for
+//               bf16 top-p alone the listed elements and value counts
+//                                                             (sampler only)
+//   queue       (1 + R_cap entries of 16 bytes) rows left for exact selects
+//               over the whole row (count first)                 (sampler only)
 constexpr int kWsCandCap = 512;
-constexpr int kWsBins = 128;
 
 // Everything one verify launch needs (passed by value to the row kernel).
 struct VerifyParams {
@@ -68,11 +69,10 @@ struct VerifyParams {
     uint32_t *ws_rticket;        // [R_cap] arrivals per row (zero between calls)
     void *ws_info;               // [R_cap] row records (64 bytes each)
     void *ws_part;               // [R_cap * nchunk] chunk partials (32 bytes each)
-    float *ws_bins;              // [R_cap * nchunk * kWsBins]
     void *ws_cand;               // [R_cap * nchunk * kWsCandCap] (value, index) pairs
-    int32_t *ws_hrows;           // [1 + R_cap] rows queued for a second pass (count first)
+    int4 *ws_queue;              // [1 + R_cap] {row, max bits, argmax, 0}; .x of entry 0 = count
     int32_t nchunk;              // chunks per row
-    int32_t n_rows;              // rows of the grid
+    int32_t n_rows;              // rows of the work (R_cap; draft rows for the confidence)
 };
 
 struct AllocParams {
@@ -107,7 +107,7 @@ size_t max_row_bytes();
 // chunks per row for a vocabulary of V elements of `elt` bytes
 int chunks_per_row(int32_t V, int elt);
 
-// workspace bytes of the row kernel (sampling adds bins and candidate lists)
+// workspace bytes of the row kernel (sampling adds the candidate lists)
 size_t row_workspace_bytes(int32_t R_cap, int32_t B, int32_t V, int elt, bool sampling);
 
 }  // namespace specv
