@@ -11,7 +11,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "libspecverify.so")
-SOURCES = ["verify.cu", "draft.cu", "capi.cu", "step_policy.cpp"]
+SOURCES = ["verify.cu", "rows.cu", "draft.cu", "capi.cu", "step_policy.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

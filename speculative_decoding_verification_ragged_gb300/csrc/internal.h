@@ -92,6 +92,8 @@ struct AllocParams {
 
 // Host launchers (return cudaError_t of the launch).
 cudaError_t launch_verify(int mode, int dtype, const VerifyParams &p, cudaStream_t stream);
+// the row path of relaxed top-K (bf16, large batches; called by launch_verify)
+cudaError_t launch_relaxed_rows(const VerifyParams &p, cudaStream_t stream);
 cudaError_t launch_alloc(const AllocParams &p, cudaStream_t stream);
 cudaError_t launch_restore_rows(const void *src, int64_t src_ld, int32_t R_cap,
                                 const int32_t *cu_rows, int32_t B, int32_t k_max,

@@ -20,7 +20,7 @@
 namespace specv {
 
 constexpr int kCandCap = kWsCandCap;    // candidates one chunk may store
-constexpr int kListCap = 3584;          // candidates a finishing CTA stages on chip
+constexpr int kListCap = 2048;          // candidates a finishing CTA stages on chip
 constexpr int kTally = 128;             // bf16 values a top-p tally over the survivors covers
 constexpr int kRowStage = 16 * 1024;    // bytes per stage when a CTA streams a whole row
 constexpr int kPureListK = 64;          // fp32 top-p alone: candidates above the 64-th thread maximum
@@ -75,6 +75,109 @@ struct Cand {
     float v;
     int32_t i;
 };
+
+// bf16 value of a 16-bit order-preserving key
+__device__ __forceinline__ float key16_value(uint32_t k)
+{
+    return key_value((k << 16) | ((k & 0x8000u) ? 0u : 0xFFFFu));
+}
+
+// ------------------------------------------------------ row records -----
+
+// Outputs of request b when its row range is not valid (cu_rows[0] != 0, an
+// empty or over-long request, or rows past R_cap): nothing accepted, no next
+// token, -1 tokens, and the BAD_ROWS status bit.  One thread per request.
+__device__ __forceinline__ void bad_request_outputs(const VerifyParams &p, int b)
+{
+    if (b >= p.B) return;
+    const int32_t c0 = __ldg(p.cu_rows), lo = __ldg(p.cu_rows + b), hi = __ldg(p.cu_rows + b + 1);
+    const int32_t n = hi - lo;
+    if (c0 != 0 || n < 1 || n - 1 > p.k_max || hi > p.R_cap) {
+        p.accepted_len[b] = 0;
+        p.next_token[b] = -1;
+        for (int j = 0; j <= p.k_max; ++j) p.out_tokens[static_cast<int64_t>(b) * (p.k_max + 1) + j] = -1;
+        set_status(p.status, SPEC_STATUS_BAD_ROWS);
+    }
+}
+
+// The row record of packed row r, computed by one full warp (every lane
+// returns it): the owner request (largest b with cu_rows[b] <= r, a 32-way
+// search), position, validity and the owner's parameters.  With a
+// confidence margin it also decides whether the margin applies to the row
+// (position, generated-token count, a warp scan of the protected ids) and
+// records the draft's logit (NaN if not); relaxed top-K records the draft's
+// logit.
+template <typename TIn, int MODE>
+__device__ RowInfo row_record(const VerifyParams &p, int r)
+{
+    using E = Elt<TIn>;
+    const int lane = threadIdx.x & 31;
+    RowInfo inf;
+    inf.sel = 0; inf.bad = 0; inf.zd = INFINITY; inf.K = 1;
+    inf.T = 0.f; inf.top_k = 0; inf.top_p = 1.f; inf.min_p = 0.f;
+    inf.seed_lo = inf.seed_hi = inf.rid = 0;
+    int lo = 0, hi = p.B - 1;
+    while (hi > lo) {
+        const int step = (hi - lo + 31) / 32;
+        const int idx = min(lo + lane * step, hi);
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, __ldg(p.cu_rows + idx) <= r);
+        const int L = m ? 31 - __clz(m) : 0;
+        const int nlo = min(lo + L * step, hi);
+        const int nhi = (L == 31) ? hi : min(lo + (L + 1) * step - 1, hi);
+        lo = nlo;
+        hi = nhi;
+    }
+    const int b = lo;
+    const int32_t c0 = __ldg(p.cu_rows), rb = __ldg(p.cu_rows + b), re = __ldg(p.cu_rows + b + 1);
+    inf.b = b;
+    inf.pos = r - rb;
+    inf.k_b = re - rb - 1;
+    inf.valid = (c0 == 0 && rb <= r && r < re && inf.k_b >= 0 && inf.k_b <= p.k_max && re <= p.R_cap);
+    inf.draft = __ldg(p.draft_ids + r);
+    if (MODE == MODE_SAMPLE) {
+        float T = __ldg(p.temperature + b), tp = __ldg(p.top_p + b), mp = __ldg(p.min_p + b);
+        int32_t tk = __ldg(p.top_k + b);
+        if (!(T >= 0.f) || isinf(T)) { inf.bad |= SPEC_STATUS_BAD_TEMPERATURE; T = 0.f; }
+        if (tk < 0) { inf.bad |= SPEC_STATUS_BAD_TOP_K; tk = 0; }
+        if (!(tp > 0.f && tp <= 1.f)) { inf.bad |= SPEC_STATUS_BAD_TOP_P; tp = 1.f; }
+        if (!(mp >= 0.f && mp <= 1.f)) { inf.bad |= SPEC_STATUS_BAD_MIN_P; mp = 0.f; }
+        inf.T = T; inf.top_k = tk; inf.top_p = tp; inf.min_p = mp;
+        const uint64_t sd = __ldg(reinterpret_cast<const unsigned long long *>(p.seed) + b);
+        inf.seed_lo = static_cast<uint32_t>(sd);
+        inf.seed_hi = static_cast<uint32_t>(sd >> 32);
+        inf.rid = p.request_id ? __ldg(p.request_id + b) : static_cast<uint32_t>(b);
+    }
+    if (MODE == MODE_GREEDY && p.margin) {
+        // the margin applies to a draft row at an eligible position whose
+        // draft is in the vocabulary and not protected; elsewhere zd is NaN,
+        // which fails the gap test in the finish
+        const float mg = __ldg(p.margin + b);
+        if (isnan(mg)) inf.bad |= SPEC_STATUS_BAD_MARGIN;
+        const int32_t gen = p.generated ? __ldg(p.generated + b) : 0;
+        const int32_t d = inf.draft;
+        bool elig = inf.valid && inf.pos < inf.k_b && d >= 0 && d < p.V && !isnan(mg) &&
+                    inf.pos >= p.from_position &&
+                    static_cast<int64_t>(gen) + inf.pos >= static_cast<int64_t>(p.after_tokens);
+        if (elig && p.n_protected > 0) {
+            bool hit = false;
+            for (int i = lane; i < p.n_protected; i += 32) hit |= (__ldg(p.protected_ids + i) == d);
+            elig = !__any_sync(0xFFFFFFFFu, hit);
+        }
+        inf.zd = __int_as_float(0x7FC00000);
+        if (elig) {
+            const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
+            inf.zd = E::load(row, d);
+        }
+    }
+    if (MODE == MODE_RELAXED) {
+        int32_t K = __ldg(p.relaxed_k + b);
+        if (K < 1) { inf.bad |= SPEC_STATUS_BAD_RELAXED_K; K = 1; }
+        inf.K = K;
+        const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
+        if (inf.draft >= 0 && inf.draft < p.V) inf.zd = E::load(row, inf.draft);
+    }
+    return inf;
+}
 
 // ------------------------------------------------------------ helpers -----
 
@@ -389,16 +492,21 @@ struct GumbelScorer {
 // chunk of only -inf reports -inf.
 constexpr float kSentinel = -1.0e38f;
 
-template <typename E, int MODE, bool SUM>
+//
+// With TOP2 it also gives the thread's second largest element (tsec; equal
+// to the maximum when the maximum repeats): the largest of the other
+// vectors' maxima, or of the maximum's vector without its first maximum.
+template <typename E, int MODE, bool SUM, bool TOP2 = false>
 __device__ __forceinline__ float pass1(const uint4 *body, int nb, int a0, float zd, int32_t &targ,
-                                       float &tsum, int32_t &tcnt)
+                                       float &tsum, int32_t &tcnt, float *tsec = nullptr)
 {
     constexpr int VEC = E::VEC;
-    float tmax = kSentinel;
+    float tmax = kSentinel, t2 = kSentinel;
     int jmax = -1;
 #pragma unroll 4
     for (int i = threadIdx.x, j = 0; i < nb; i += kThreads, ++j) {
         const float vm = E::vmax(body[i]);
+        if (TOP2) t2 = fmaxf(t2, fminf(vm, tmax));
         jmax = (vm > tmax) ? j : jmax;
         tmax = fmaxf(tmax, vm);
     }
@@ -411,7 +519,13 @@ __device__ __forceinline__ float pass1(const uint4 *body, int nb, int a0, float 
         for (int q = VEC - 1; q >= 0; --q)
             if (x[q] == tmax) first = q;
         targ = a0 + i * VEC + first;
+        if (TOP2) {
+#pragma unroll
+            for (int q = 0; q < VEC; ++q)
+                if (q != first) t2 = fmaxf(t2, x[q]);
+        }
     }
+    if (TOP2) *tsec = (t2 == kSentinel) ? -INFINITY : t2;
     if (SUM || MODE == MODE_RELAXED) {
         const float c0 = -tmax * kLog2e;
         if constexpr (E::BYTES == 2) {
@@ -797,5 +911,52 @@ __device__ bool tally_top_p(Visit &&visit, uint32_t klo, uint32_t ktop, float M,
     return true;
 }
 
+
+// The token of a sampler row filtered by top-k and / or min-p (then top-p
+// over their survivors), from a candidate list that holds every element of
+// the row at or above a bound whose key is klist (visit_lst yields them): the
+// survivors of top-k and min-p are the upper set {z >= th_S} (th_S from the
+// min-p level and an exact k-th-value select over the list); top-p keeps the
+// group where their mass, counted from the top, first reaches top_p times
+// their total (per-value tallies when the survivors span at most kTally
+// bf16 values, else an exact mass select); Gumbel-max over what is left.
+// cnt [kTally] and bst [kTally] are shared scratch.  Result in best / bi.
+template <typename E, typename Visit>
+__device__ void settle_from_list(Visit &&visit_lst, const RowInfo &info, const Filter &f, float M,
+                                 uint32_t klist, uint32_t *cnt, unsigned long long *bst,
+                                 GumbelScorer &gs, float &best, int32_t &bi, Shared &sh)
+{
+    const float sc = f.sc;
+    const uint32_t keyM = fkey(M);
+    const float th_m = f.use_m ? M + f.T * logf(info.min_p) : -INFINITY;
+    uint32_t key_S = f.use_m ? fkey(th_m) : 0u;
+    if (f.use_k)
+        key_S = max(key_S, select_key<E, false>(visit_lst, max(key_S, klist), keyM, 0.f,
+                                                static_cast<uint32_t>(info.top_k), M, sc, sh));
+    if (E::BYTES == 2 && f.use_p) {
+        // the survivors tallied per value when they span at most kTally
+        // bf16 values
+        const uint32_t klo = bf16_key_ceil(key_S), ktop = keyM >> 16;
+        if (ktop >= klo && ktop - klo < static_cast<uint32_t>(kTally)) {
+            tally_top_p(visit_lst, klo, ktop, M, sc, gs, info.top_p, 0.f, cnt, bst, best, bi, sh);
+            return;
+        }
+    }
+    uint32_t key_F = key_S;
+    if (f.use_p) {
+        float w = 0.f;
+        const uint32_t kS = key_S;
+        visit_lst([&](float v, int32_t) {
+            if (fkey(v) >= kS) w += ex2((v - M) * sc);
+        }, key_floor(key_S));
+        const float Wt = block_sum(w, sh);
+        key_F = max(key_S, select_key<E, true>(visit_lst, key_S, keyM, info.top_p * Wt, 0u, M, sc, sh));
+    }
+    const uint32_t kF = key_F;
+    visit_lst([&](float v, int32_t ix) {
+        if (fkey(v) >= kF) keep_best(gs(v, ix), ix, best, bi);
+    }, key_floor(key_F));
+    block_best(best, bi, sh);
+}
 
 }  // namespace specv

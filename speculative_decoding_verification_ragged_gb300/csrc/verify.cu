@@ -70,7 +70,7 @@ namespace specv {
 
 constexpr int kTopBins = 256;       // bf16 top-p alone: values counted at and below the chunk max
 constexpr int kFrontCap = 384;      // bf16 top-p alone: listed elements per chunk
-constexpr int kFinScratch = 32 * 1024;   // finish kernel: candidates or counts
+constexpr int kFinScratch = 20 * 1024;   // finish kernel: candidates or counts (6 CTAs per SM)
 constexpr int kExactCtas = 256;          // CTAs of the exact kernel (strided over its queue)
 
 // Element listed by a bf16 top-p-alone chunk: its Gumbel score reaches the
@@ -85,112 +85,33 @@ static_assert(kChunkBytes / 2 <= 65536, "a bf16 chunk offset fits 16 bits");
 // (bf16 top-p alone), or its thread maxima (other filtered rows)
 static_assert(kFrontCap * sizeof(Front) + kTopBins * sizeof(uint16_t) <= kCandCap * sizeof(Cand),
               "listed elements and counts fit a chunk's candidate area");
-static_assert(kThreads * sizeof(float) <= kCandCap * sizeof(Cand), "thread maxima fit");
+static_assert(kThreads * (2 * sizeof(float) + sizeof(uint16_t)) <= kCandCap * sizeof(Cand),
+              "thread maxima, second values and offsets fit");
 constexpr int kMaxStride = kCandCap * static_cast<int>(sizeof(Cand) / sizeof(float));  // floats per chunk area
 // the finish stages gathered candidates, then the survivors' tallies
 static_assert(kListCap * sizeof(Cand) + kTally * (sizeof(uint32_t) + sizeof(uint64_t)) <= kFinScratch,
               "gathered candidates and tallies fit the finish scratch");
-static_assert(kMaxChunks * kTopBins * sizeof(uint16_t) <= kFinScratch, "every chunk's counts fit");
+// bf16 top-p alone stages every chunk's counts (longer rows take the exact path)
+constexpr int kCountChunks = static_cast<int>(kFinScratch / (kTopBins * sizeof(uint16_t)));
 
 // ---------------------------------------------------------- prologue -----
-// One warp per packed row: owner request (largest b with cu_rows[b] <= r),
-// position, validity and the owner's parameters.  Extra CTAs handle the
-// requests without a valid row range.
+// One warp per packed row: its row record (row_record); extra CTAs handle
+// the requests without a valid row range (bad_request_outputs).
 template <typename TIn, int MODE>
 __global__ void __launch_bounds__(256) row_info_kernel(const VerifyParams p, int row_blocks)
 {
-    using E = Elt<TIn>;
     griddep_launch_dependents();
     // the sampler's queue of rows for exact selects starts empty (the
     // previous call's kernels have completed before this one starts)
     if (MODE == MODE_SAMPLE && blockIdx.x == 0 && threadIdx.x == 0) p.ws_queue[0].x = 0;
-    const int lane = threadIdx.x & 31;
     if (static_cast<int>(blockIdx.x) >= row_blocks) {
-        const int b = (blockIdx.x - row_blocks) * 256 + threadIdx.x;
-        if (b >= p.B) return;
-        const int32_t c0 = __ldg(p.cu_rows), lo = __ldg(p.cu_rows + b), hi = __ldg(p.cu_rows + b + 1);
-        const int32_t n = hi - lo;
-        if (c0 != 0 || n < 1 || n - 1 > p.k_max || hi > p.R_cap) {
-            p.accepted_len[b] = 0;
-            p.next_token[b] = -1;
-            for (int j = 0; j <= p.k_max; ++j) p.out_tokens[static_cast<int64_t>(b) * (p.k_max + 1) + j] = -1;
-            set_status(p.status, SPEC_STATUS_BAD_ROWS);
-        }
+        bad_request_outputs(p, (blockIdx.x - row_blocks) * 256 + threadIdx.x);
         return;
     }
     const int r = (blockIdx.x * 256 + threadIdx.x) >> 5;
     if (r >= p.R_cap) return;
-    RowInfo inf;
-    inf.sel = 0; inf.bad = 0; inf.zd = INFINITY; inf.K = 1;
-    inf.T = 0.f; inf.top_k = 0; inf.top_p = 1.f; inf.min_p = 0.f;
-    inf.seed_lo = inf.seed_hi = inf.rid = 0;
-    int lo = 0, hi = p.B - 1;
-    while (hi > lo) {
-        const int step = (hi - lo + 31) / 32;
-        const int idx = min(lo + lane * step, hi);
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, __ldg(p.cu_rows + idx) <= r);
-        const int L = m ? 31 - __clz(m) : 0;
-        const int nlo = min(lo + L * step, hi);
-        const int nhi = (L == 31) ? hi : min(lo + (L + 1) * step - 1, hi);
-        lo = nlo;
-        hi = nhi;
-    }
-    const int b = lo;
-    const int32_t c0 = __ldg(p.cu_rows), rb = __ldg(p.cu_rows + b), re = __ldg(p.cu_rows + b + 1);
-    inf.b = b;
-    inf.pos = r - rb;
-    inf.k_b = re - rb - 1;
-    inf.valid = (c0 == 0 && rb <= r && r < re && inf.k_b >= 0 && inf.k_b <= p.k_max && re <= p.R_cap);
-    inf.draft = __ldg(p.draft_ids + r);
-    if (MODE == MODE_SAMPLE) {
-        float T = __ldg(p.temperature + b), tp = __ldg(p.top_p + b), mp = __ldg(p.min_p + b);
-        int32_t tk = __ldg(p.top_k + b);
-        if (!(T >= 0.f) || isinf(T)) { inf.bad |= SPEC_STATUS_BAD_TEMPERATURE; T = 0.f; }
-        if (tk < 0) { inf.bad |= SPEC_STATUS_BAD_TOP_K; tk = 0; }
-        if (!(tp > 0.f && tp <= 1.f)) { inf.bad |= SPEC_STATUS_BAD_TOP_P; tp = 1.f; }
-        if (!(mp >= 0.f && mp <= 1.f)) { inf.bad |= SPEC_STATUS_BAD_MIN_P; mp = 0.f; }
-        inf.T = T; inf.top_k = tk; inf.top_p = tp; inf.min_p = mp;
-        const uint64_t sd = __ldg(reinterpret_cast<const unsigned long long *>(p.seed) + b);
-        inf.seed_lo = static_cast<uint32_t>(sd);
-        inf.seed_hi = static_cast<uint32_t>(sd >> 32);
-        inf.rid = p.request_id ? __ldg(p.request_id + b) : static_cast<uint32_t>(b);
-    }
-    if (MODE == MODE_GREEDY && p.margin) {
-        // the margin applies to a draft row at an eligible position whose
-        // draft is in the vocabulary and not protected; elsewhere zd is NaN,
-        // which fails the gap test in the finish
-        const float mg = __ldg(p.margin + b);
-        if (isnan(mg)) inf.bad |= SPEC_STATUS_BAD_MARGIN;
-        const int32_t gen = p.generated ? __ldg(p.generated + b) : 0;
-        const int32_t d = inf.draft;
-        bool elig = inf.valid && inf.pos < inf.k_b && d >= 0 && d < p.V && !isnan(mg) &&
-                    inf.pos >= p.from_position &&
-                    static_cast<int64_t>(gen) + inf.pos >= static_cast<int64_t>(p.after_tokens);
-        if (elig && p.n_protected > 0) {
-            bool hit = false;
-            for (int i = lane; i < p.n_protected; i += 32) hit |= (__ldg(p.protected_ids + i) == d);
-            elig = !__any_sync(0xFFFFFFFFu, hit);
-        }
-        inf.zd = __int_as_float(0x7FC00000);
-        if (elig) {
-            const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
-            inf.zd = E::load(row, d);
-        }
-    }
-    if (MODE == MODE_RELAXED) {
-        int32_t K = __ldg(p.relaxed_k + b);
-        if (K < 1) { inf.bad |= SPEC_STATUS_BAD_RELAXED_K; K = 1; }
-        inf.K = K;
-        const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
-        if (inf.draft >= 0 && inf.draft < p.V) inf.zd = E::load(row, inf.draft);
-    }
-    if (lane == 0) reinterpret_cast<RowInfo *>(p.ws_info)[r] = inf;
-}
-
-// bf16 value of a 16-bit order-preserving key
-__device__ __forceinline__ float key16_value(uint32_t k)
-{
-    return key_value((k << 16) | ((k & 0x8000u) ? 0u : 0xFFFFu));
+    const RowInfo inf = row_record<TIn, MODE>(p, r);
+    if ((threadIdx.x & 31) == 0) reinterpret_cast<RowInfo *>(p.ws_info)[r] = inf;
 }
 
 // Mass of the staged chunk at temperature T: sum exp((z - m_c) / T) over
@@ -327,7 +248,7 @@ __device__ void summary_top_p_bf16(const VerifyParams &p, const uint4 *body, con
 template <typename E>
 __device__ void summary_sampler(const VerifyParams &p, const RowInfo &info, const uint4 *body,
                                 const ChunkGeom &g, float thread_max, int32_t thread_arg,
-                                int64_t rc, Shared &sh)
+                                float thread_sec, int64_t rc, Shared &sh)
 {
     constexpr int VEC = E::VEC;
     const int tid = threadIdx.x;
@@ -371,11 +292,15 @@ __device__ void summary_sampler(const VerifyParams &p, const RowInfo &info, cons
             return;
         }
     }
-    // top-k / min-p, fp32 top-p alone: the thread maxima (the thread's
-    // elements of the chunk, extras included), and for fp32 top-p alone the
+    // top-k / min-p, fp32 top-p alone: per thread slot (the thread's elements
+    // of the chunk, extras included) its maximum, its second largest element
+    // and the maximum's offset in the chunk; for fp32 top-p alone also the
     // chunk's mass at temperature T
     float *mx = reinterpret_cast<float *>(reinterpret_cast<Cand *>(p.ws_cand) + rc * kCandCap);
     mx[tid] = thread_max;
+    mx[kThreads + tid] = thread_sec;
+    reinterpret_cast<uint16_t *>(mx + 2 * kThreads)[tid] =
+        static_cast<uint16_t>(thread_max > -INFINITY ? thread_arg - g.e0 : 0);
     if (f.pure_p && m_c > -INFINITY) {
         float mass = (T != 1.0f) ? chunk_mass<E>(body, g.nb, m_c, f.sc) : 0.f;
         if (T != 1.0f && tid < g.n_extra) mass += ex2((sh.extras_v[tid] - m_c) * f.sc);
@@ -469,20 +394,32 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
                           (MODE == MODE_SAMPLE && info.T == 1.0f && info.top_p < 1.f &&
                            !(info.top_k > 0 && info.top_k < p.V) && !(info.min_p > 0.f));
     const float zd = info.zd;
-    float tmax = -INFINITY, tsum = 0.f;
+    float tmax = -INFINITY, tsum = 0.f, tsec = -INFINITY;
     int32_t targ = INT_MAX, tcnt = 0;
-    if (need_sum) tmax = pass1<E, MODE, true>(body, g.nb, g.a0, zd, targ, tsum, tcnt);
-    else tmax = pass1<E, MODE, false>(body, g.nb, g.a0, zd, targ, tsum, tcnt);
-    if (tid < g.n_extra)
+    // sampler rows bounded by top-k / min-p (and fp32 top-p alone) keep each
+    // thread's two largest elements
+    const bool top2 = MODE == MODE_SAMPLE && info.T > 0.f &&
+                      ((info.top_k > 0 && info.top_k < p.V) || info.min_p > 0.f ||
+                       (E::BYTES == 4 && info.top_p < 1.f));
+    if (MODE == MODE_SAMPLE && top2) {
+        if (need_sum) tmax = pass1<E, MODE, true, true>(body, g.nb, g.a0, zd, targ, tsum, tcnt, &tsec);
+        else tmax = pass1<E, MODE, false, true>(body, g.nb, g.a0, zd, targ, tsum, tcnt, &tsec);
+    } else {
+        if (need_sum) tmax = pass1<E, MODE, true>(body, g.nb, g.a0, zd, targ, tsum, tcnt);
+        else tmax = pass1<E, MODE, false>(body, g.nb, g.a0, zd, targ, tsum, tcnt);
+    }
+    if (tid < g.n_extra) {
+        tsec = fmaxf(tsec, fminf(xe, tmax));
         combine(tmax, targ, tsum, tcnt, xe, ie, 1.f, (MODE == MODE_RELAXED && xe > zd) ? 1 : 0,
                 need_sum);
+    }
     const float thread_max = tmax;
     const int32_t thread_arg = targ;
     chunk_reduce<MODE>(tmax, targ, tsum, tcnt, need_sum, sh);
 
     const int64_t rc = static_cast<int64_t>(r) * nchunk + c;
     if (MODE == MODE_SAMPLE && info.T > 0.f) {
-        summary_sampler<E>(p, info, body, g, thread_max, thread_arg, rc, sh);
+        summary_sampler<E>(p, info, body, g, thread_max, thread_arg, tsec, rc, sh);
         csync();
     }
     if (tid == 0) reinterpret_cast<ChunkPart *>(p.ws_part)[rc] = sh.part;
@@ -556,6 +493,7 @@ __device__ bool finish_top_p_bf16(const VerifyParams &p, const RowInfo &info, co
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const Filter f(info, p.V);
     const uint32_t KT = fkey(M) >> 16;
+    if (nchunk > kCountChunks) return false;
     if (warp == 0) {
         float w = 0.f;
         uint32_t kc = 0u;
@@ -644,14 +582,14 @@ __device__ __forceinline__ void stage_maxima(const VerifyParams &p, int r, float
 }
 
 // Every element of row r with a value at or above L, into lst (count in
-// sh.cand_n; above cap the list is incomplete).  The thread slots (chunk q,
-// thread t) whose recorded maximum (staged in mxs) reaches L are collected
-// into a flat list in shared memory; then each thread reads one 16-byte
-// vector of those slots at a time from the logits, so every load of the row
-// goes out in one batch.  Head / tail elements of a slot come with its first
-// vector.
+// sh.cand_n; above cap the list is incomplete).  A thread slot (chunk q,
+// thread t) whose recorded maximum (staged in mxs) reaches L contributes that
+// maximum from its record; the few slots whose second largest element
+// reaches L as well are collected into a flat list in shared memory and read
+// back whole, one 16-byte vector per thread at a time, so their loads go out
+// in one batch.  Head / tail elements of a slot come with its first vector.
 template <typename E, typename TIn>
-__device__ void gather_above(const VerifyParams &p, const TIn *row, float L, const float *mxs,
+__device__ void gather_above(const VerifyParams &p, int r, const TIn *row, float L, const float *mxs,
                              Cand *lst, int cap, int *slots, int slot_cap, Shared &sh)
 {
     constexpr int VEC = E::VEC;
@@ -660,11 +598,29 @@ __device__ void gather_above(const VerifyParams &p, const TIn *row, float L, con
     const int nchunk = p.nchunk;
     if (tid == 0) { sh.cand_n = 0; sh.total = 0; }
     csync();
-    for (int q = 0; q < nchunk; ++q)
-        if (mxs[q * kThreads + tid] >= L) {
+    auto add = [&](float v, int32_t ix) {
+        const int slot = warp_append(&sh.cand_n);
+        if (slot < cap) { lst[slot].v = v; lst[slot].i = ix; }
+    };
+    // a slot whose maximum reaches L gives that maximum (value and offset
+    // are recorded); only a slot whose second largest element reaches L too
+    // is read back whole
+    const float *mxr = reinterpret_cast<const float *>(reinterpret_cast<const Cand *>(p.ws_cand) +
+                                                       static_cast<int64_t>(r) * nchunk * kCandCap);
+    constexpr int CE = kChunkBytes / E::BYTES;
+    for (int q = 0; q < nchunk; ++q) {
+        const float m = mxs[q * kThreads + tid];
+        if (!(m >= L)) continue;
+        const float *area = mxr + static_cast<int64_t>(q) * kMaxStride;
+        const float sv = __ldcg(area + kThreads + tid);
+        const uint16_t a = __ldcg(reinterpret_cast<const unsigned short *>(area + 2 * kThreads) + tid);
+        if (sv >= L) {
             const int k = warp_append(&sh.total);
             if (k < slot_cap) slots[k] = q * kThreads + tid;
+        } else {
+            add(m, q * CE + static_cast<int32_t>(a));
         }
+    }
     csync();
     const int ns = sh.total;
     if (ns > slot_cap) {                 // far too many: the caller falls back
@@ -672,10 +628,6 @@ __device__ void gather_above(const VerifyParams &p, const TIn *row, float L, con
         csync();
         return;
     }
-    auto add = [&](float v, int32_t ix) {
-        const int slot = warp_append(&sh.cand_n);
-        if (slot < cap) { lst[slot].v = v; lst[slot].i = ix; }
-    };
     for (int e = tid; e < ns * PER; e += kThreads) {
         const int sl = slots[e / PER], j = e - (e / PER) * PER;
         const int q = sl / kThreads, t = sl - q * kThreads;
@@ -832,7 +784,7 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
             // candidates: slots from the top, candidates from the bottom
             constexpr int kSlotCap = 1024;
             static_assert(kListCap * sizeof(Cand) + kSlotCap * sizeof(int) <= kFinScratch, "slots fit");
-            gather_above<E, TIn>(p, row, L, mxs, lst, kListCap,
+            gather_above<E, TIn>(p, r, row, L, mxs, lst, kListCap,
                                  reinterpret_cast<int *>(scratch + kFinScratch) - kSlotCap, kSlotCap, sh);
             const int n_list = sh.cand_n;
             auto visit_lst = [&](auto &&fn, float thr) {
@@ -873,41 +825,9 @@ __global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParam
                 }
             } else {
                 // ---- top-k and / or min-p (then top-p over the survivors) --
-                uint32_t key_S = f.use_m ? fkey(th_m) : 0u;
-                if (f.use_k)
-                    key_S = max(key_S, select_key<E, false>(visit_lst, max(key_S, fkey(L)), keyM, 0.f,
-                                                            static_cast<uint32_t>(info.top_k), M,
-                                                            sc, sh));
-                bool tallied = false;
-                if (E::BYTES == 2 && f.use_p) {
-                    // the survivors tallied per value when they span at most
-                    // kTally bf16 values
-                    const uint32_t klo = bf16_key_ceil(key_S), ktop = keyM >> 16;
-                    if (ktop >= klo && ktop - klo < static_cast<uint32_t>(kTally)) {
-                        uint32_t *cnt = reinterpret_cast<uint32_t *>(lst + kListCap);
-                        tally_top_p(visit_lst, klo, ktop, M, sc, gs, info.top_p, 0.f, cnt,
-                                    reinterpret_cast<unsigned long long *>(cnt + kTally), best, bi, sh);
-                        tallied = true;
-                    }
-                }
-                if (!tallied) {
-                    uint32_t key_F = key_S;
-                    if (f.use_p) {
-                        float w = 0.f;
-                        const uint32_t kS = key_S;
-                        visit_lst([&](float v, int32_t) {
-                            if (fkey(v) >= kS) w += ex2((v - M) * sc);
-                        }, key_floor(key_S));
-                        const float Wt = block_sum(w, sh);
-                        key_F = max(key_S, select_key<E, true>(visit_lst, key_S, keyM, info.top_p * Wt,
-                                                               0u, M, sc, sh));
-                    }
-                    const uint32_t kF = key_F;
-                    visit_lst([&](float v, int32_t ix) {
-                        if (fkey(v) >= kF) score_all(v, ix);
-                    }, key_floor(key_F));
-                    block_best(best, bi, sh);
-                }
+                uint32_t *cnt = reinterpret_cast<uint32_t *>(lst + kListCap);
+                settle_from_list<E>(visit_lst, info, f, M, fkey(L), cnt,
+                                    reinterpret_cast<unsigned long long *>(cnt + kTally), gs, best, bi, sh);
             }
         }
         if (whole && tid == 0) {
@@ -1112,8 +1032,32 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     return cudaLaunchKernelEx(&cx, exact_rows_kernel<TIn>, p);
 }
 
+// Rows at or above which bf16 relaxed top-K verification takes the row
+// path (one CTA per row): twice the SM count, so that the row CTAs fill the
+// GPU.  Greedy rows stay on the chunk path, which measured faster for them.
+static cudaError_t row_path_threshold(int &rows)
+{
+    static int sms[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!sms[dev]) {
+        e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    rows = 2 * sms[dev];
+    return cudaSuccess;
+}
+
 cudaError_t launch_verify(int mode, int dtype, const VerifyParams &p, cudaStream_t stream)
 {
+    if (dtype == SPEC_BF16 && mode == MODE_RELAXED) {
+        int th = 0;
+        const cudaError_t e = row_path_threshold(th);
+        if (e != cudaSuccess) return e;
+        if (p.R_cap >= th) return launch_relaxed_rows(p, stream);
+    }
     if (dtype == SPEC_BF16) {
         switch (mode) {
         case MODE_GREEDY: return launch_t<uint16_t, MODE_GREEDY>(p, stream);
