@@ -444,6 +444,76 @@ def time_entry_points(sv, dev, stream, args) -> dict:
     out["spec_draft_confidence"] = {"workload": "B=16 k=7 V=151552 bf16, threshold 0.3",
                                     "rows": rows, "us": round(ms * 1e3, 2),
                                     "hbm_gbs": round(rows * db.V * 2 / (ms * 1e-3) / 1e9, 1)}
+    # the adaptive pipeline on the device: confidence -> allocation -> packed
+    # greedy verification of the allocated rows (target logits B*(k+1) x V)
+    tsets = [bf(db.target_logits) for _ in range(8)]
+    tws = sv.new_workspace(cap, db.B, db.V, torch.bfloat16, dev)
+    tb = Bd.Batch(tsets[0].data_ptr(), Bd.SPEC_BF16, db.V, tsets[0].stride(0), db.B, db.k, cap,
+                  bufs[3].data_ptr(), bufs[6].data_ptr())
+    to, tres = Bd._outputs(db.B, db.k, cap, dev, False, None)
+
+    def pipeline(i):
+        d.draft_logits = dsets[i % 8].data_ptr()
+        ok(L.spec_draft_confidence(C.byref(d), C.byref(a), dws.data_ptr(), dws.numel(), s))
+        tb.logits = tsets[i % 8].data_ptr()
+        ok(L.spec_verify_greedy(C.byref(tb), C.byref(to), tws.data_ptr(), tws.numel(), s))
+    for i in range(5):
+        pipeline(i)
+    ms = _time_launches(pipeline, n, stream)
+    vrows = int(bufs[7].cpu()[0])
+    out["adaptive_pipeline"] = {
+        "workload": "B=16 k=7 V=151552 bf16: spec_draft_confidence (threshold 0.3) then "
+                    "spec_verify_greedy over the allocated packed rows",
+        "draft_rows": rows, "verified_rows": vrows, "us": round(ms * 1e3, 2),
+        "hbm_gbs": round((rows + vrows) * db.V * 2 / (ms * 1e-3) / 1e9, 1),
+        "mean_accepted": round(float(tres["accepted_len"].float().mean()), 3)}
+    del dsets, tsets
+    # tiny greedy verification: 4 requests, k=4, vocab 1024, fp32 (launch-
+    # and latency-bound; the 80 KB input stays in L2)
+    vt = W.tiny_greedy()
+    lt = torch.from_numpy(vt.logits).to(dev)
+    cu, dr = torch.from_numpy(vt.cu_rows).to(dev), torch.from_numpy(vt.draft_ids).to(dev)
+    ws = sv.new_workspace(vt.R, vt.B, vt.V, torch.float32, dev)
+    b = Bd._batch(lt, vt.V, vt.B, vt.k_max, vt.R, cu, dr)
+    o, _ = Bd._outputs(vt.B, vt.k_max, vt.R, dev, False, None)
+
+    def tiny(i):
+        ok(L.spec_verify_greedy(C.byref(b), C.byref(o), ws.data_ptr(), ws.numel(), s))
+    for i in range(5):
+        tiny(i)
+    ms = _time_launches(tiny, n, stream)
+    out["spec_verify_greedy_tiny"] = {"workload": "B=4 k=4 V=1024 fp32 (20 rows), L2-resident",
+                                      "rows": vt.R, "us": round(ms * 1e3, 2)}
+    # relaxed top-K over 20 seeded steps, the prefix-acceptance counters
+    # accumulated on the device by the fused path
+    steps = []
+    for vb in W.relaxed_steps(20):
+        steps.append((bf(vb.logits), torch.from_numpy(vb.cu_rows).to(dev),
+                      torch.from_numpy(vb.draft_ids).to(dev)))
+    K = torch.from_numpy(vb.extra["relaxed_k"]).to(dev)
+    ws = sv.new_workspace(vb.R, vb.B, vb.V, torch.bfloat16, dev)
+    acc = torch.zeros(vb.k_max, dtype=torch.int64, device=dev)
+    ver, hist = acc.clone(), torch.zeros(vb.k_max + 1, dtype=torch.int64, device=dev)
+    o, _ = Bd._outputs(vb.B, vb.k_max, vb.R, dev, False, (acc, ver, hist))
+    bs = [Bd._batch(lg, vb.V, vb.B, vb.k_max, vb.R, c_, d_) for lg, c_, d_ in steps]
+
+    def step(i):
+        ok(L.spec_verify_relaxed_topk(C.byref(bs[i]), K.data_ptr(), C.byref(o), ws.data_ptr(),
+                                      ws.numel(), s))
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    for x in (acc, ver, hist):
+        x.zero_()
+    ms = _time_launches(step, len(steps), stream)
+    a_, v_ = acc.cpu().numpy(), ver.cpu().numpy()
+    out["relaxed_20_steps"] = {
+        "workload": "EAGLE-relaxed B=256 k=5 V=152064 bf16 K=4, 20 seeded steps, fused counters",
+        "steps": len(steps), "rows_per_step": vb.R, "us_per_step": round(ms * 1e3, 2),
+        "hbm_gbs": round(vb.R * vb.V * 2 / (ms * 1e-3) / 1e9, 1),
+        "prefix_acceptance": [round(float(x) / max(float(y), 1.0), 4) for x, y in zip(a_, v_)],
+        "accepted_hist": [int(x) for x in hist.cpu().numpy()]}
+    del steps, bs
     # standalone prefix statistics
     al = torch.randint(0, 5, (128,), dtype=torch.int32, device=dev)
     cu = torch.arange(0, 129 * 5, 5, dtype=torch.int32, device=dev)

@@ -177,12 +177,14 @@ SPEC_API int spec_verify_greedy(const spec_batch *batch, const spec_outputs *out
  * workspace (spec_workspace_bytes(R_cap, B, V, dtype, 0)) exceeds
  * SPEC_NOALLOC_SCRATCH_BYTES returns SPEC_ERR_WORKSPACE before any launch
  * (about 250 KiB suffice for 640 rows of a 152064-token vocabulary).
- * The first call on each device looks up the array's device address (with
- * that device current), so make that first call before any stream capture.
- * Every call shares the one array: calls that can overlap on the GPU (two
- * streams, two host threads) race and must be ordered by the caller.  Each
- * call clears the array's ticket words itself on its stream before its
- * kernels run.  Nothing is allocated or freed.
+ * Every call looks up the array's device address in the current context
+ * (cudaGetSymbolAddress), so the address is never stale after a device
+ * reset or under a non-primary context.  The array used is the current
+ * device's: the inputs and outputs must be on that device (the Python
+ * binding refuses a mismatch).  Every call shares the one array: calls that
+ * can overlap on the GPU (two streams, two host threads) race and must be
+ * ordered by the caller.  Each call clears the array's ticket words itself
+ * on its stream before its kernels run.  Nothing is allocated or freed.
  */
 #define SPEC_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
 SPEC_API int spec_verify_greedy_noalloc(const spec_batch *batch, const spec_outputs *out,

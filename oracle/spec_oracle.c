@@ -31,7 +31,7 @@
  *   [Philox] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
  *            1, 2, 3", SC'11 -- the Philox4x32 bijection with 10 rounds.
  *
- * Readings where the pages are silent (each listed in the design doc):
+ * Readings where the pages are silent:
  *   - argmax ties: lowest index; -0.0 equals +0.0.
  *   - filter order: temperature, then top-k and min-p as value thresholds
  *     (they commute), then top-p over their survivors; ties at a threshold

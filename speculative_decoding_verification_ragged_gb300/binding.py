@@ -263,7 +263,15 @@ def verify_greedy_noalloc(logits, cu_rows, draft_ids, *, V: int, B: int, k_max: 
                           stream=None) -> dict:
     """spec_verify_greedy_noalloc: greedy verification for callers that cannot
     allocate device memory; the library's built-in scratch array stands in
-    for the workspace.  Calls that overlap on the GPU race on that array."""
+    for the workspace.  Calls that overlap on the GPU race on that array.
+    The array used is the current device's, so logits must be on it."""
+    if logits.device.type != "cuda":
+        raise SpecError("verify_greedy_noalloc: logits must be a CUDA tensor, got %s" % logits.device)
+    cur = torch.cuda.current_device()
+    if logits.device.index != cur:
+        raise SpecError("verify_greedy_noalloc: logits are on %s but the current device is "
+                        "cuda:%d (the built-in scratch array is the current device's)"
+                        % (logits.device, cur))
     L = load_library()
     R_cap = R_cap or B * (k_max + 1)
     b = _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids)

@@ -4,7 +4,6 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -137,27 +136,20 @@ int run_verify(int mode, const spec_batch *b, VerifyParams &p, cudaStream_t s)
 }
 
 // Built-in scratch of spec_verify_greedy_noalloc: a device array of the
-// library (zero at load), its device address looked up once per device.
+// library (zero at load).
 static __device__ __align__(256) uint8_t g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[64] = {};
 
-// Device address of the scratch array on the current device (the host-side
+// Device address of the scratch array in the current context (the host-side
 // name of the array is not a device address; only this lookup gives one).
+// Looked up on every call, never cached: after a device reset, or under a
+// context other than the device's primary one, the module is loaded again
+// and the array can move.
 int noalloc_scratch(void **ptr)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (dev < 0 || dev >= 64) return SPEC_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e);
-        g_noalloc_ptr[dev] = p;
-    }
-    *ptr = g_noalloc_ptr[dev];
+    *ptr = p;
     return SPEC_OK;
 }
 

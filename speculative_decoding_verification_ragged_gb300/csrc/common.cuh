@@ -292,18 +292,61 @@ template <> struct Elt<float> {
 // Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, SC'11): each round
 // multiplies counter words 0 and 2 by fixed odd constants, swaps the
 // halves, and mixes in the round key; the key advances by Weyl increments.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u, kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u, kPhiloxW1 = 0xBB67AE85u;
+
+// the 64-bit product of two words as (lo, hi): one wide multiply
+__device__ __forceinline__ void mulhilo32(uint32_t a, uint32_t b, uint32_t &lo, uint32_t &hi)
 {
-#pragma unroll
-    for (int i = 0; i < 10; ++i) {
-        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
-    }
-    return c;
+    const uint64_t m = static_cast<uint64_t>(a) * b;
+    lo = static_cast<uint32_t>(m);
+    hi = static_cast<uint32_t>(m >> 32);
 }
+
+// Philox4x32-10 blocks for counters (ctr, w1, w2, w3) in which only ctr
+// varies.  Round 0 multiplies word 2 (= w2) and round 1 multiplies word 0
+// (a function of w1, w2 and the key alone), so those two products and the
+// words they feed are fixed per (w1, w2, w3, key) and computed once; a
+// block then costs two wide multiplies for rounds 0-1 and two per later
+// round.  Identical output to the round-by-round definition.
+struct Philox {
+    uint32_t C, D, E, F;        // words entering rounds 0-1 that do not depend on ctr
+    uint32_t k0, k1;            // the key of round 2
+    __device__ __forceinline__ static Philox make(uint32_t w1, uint32_t w2, uint32_t w3,
+                                                  uint32_t key0, uint32_t key1)
+    {
+        Philox q;
+        uint32_t lo, hi;
+        mulhilo32(kPhiloxM1, w2, lo, hi);               // round 0, word 2
+        const uint32_t A = hi ^ w1 ^ key0;              // round 0 output word 0
+        q.C = w3 ^ key1;                                // xored into round 0 output word 2
+        uint32_t loA, hiA;
+        mulhilo32(kPhiloxM0, A, loA, hiA);              // round 1, word 0
+        q.D = lo ^ (key0 + kPhiloxW0);                  // round 1 output word 0 = hi(M1 x) ^ D
+        q.E = hiA ^ (key1 + kPhiloxW1);                 // round 1 output word 2 = lo0 ^ E
+        q.F = loA;                                      // round 1 output word 3
+        q.k0 = key0 + 2u * kPhiloxW0;
+        q.k1 = key1 + 2u * kPhiloxW1;
+        return q;
+    }
+    __device__ __forceinline__ uint4 operator()(uint32_t ctr) const
+    {
+        uint32_t lo0, hi0, lo1, hi1;
+        mulhilo32(kPhiloxM0, ctr, lo0, hi0);            // round 0, word 0
+        mulhilo32(kPhiloxM1, hi0 ^ C, lo1, hi1);        // round 1, word 2
+        uint4 c = make_uint4(hi1 ^ D, lo1, lo0 ^ E, F);
+        uint32_t a = k0, b = k1;
+#pragma unroll
+        for (int i = 2; i < 10; ++i) {
+            mulhilo32(kPhiloxM0, c.x, lo0, hi0);
+            mulhilo32(kPhiloxM1, c.z, lo1, hi1);
+            c = make_uint4(hi1 ^ c.y ^ a, lo1, hi0 ^ c.w ^ b, lo0);
+            a += kPhiloxW0;
+            b += kPhiloxW1;
+        }
+        return c;
+    }
+};
 
 __device__ __forceinline__ uint32_t word_of(uint4 v, uint32_t w)
 {

@@ -419,11 +419,14 @@ __device__ __forceinline__ bool kth_level(float thread_max, float m_c, int k, fl
 // Philox4x32-10 stream of one row: counter (i >> 2, position, request id,
 // step), key (seed lo, seed hi); element i takes word i & 3.
 struct Noise {
-    uint32_t pos, rid, step, k0, k1;
-    __device__ __forceinline__ uint4 block(uint32_t ctr) const
+    Philox ph;
+    // counter (i >> 2, position, request id, step), key = the 64-bit seed
+    __device__ __forceinline__ Noise(uint32_t pos, uint32_t rid, uint32_t step, uint32_t seed_lo,
+                                     uint32_t seed_hi)
+        : ph(Philox::make(pos, rid, step, seed_lo, seed_hi))
     {
-        return philox4x32_10(make_uint4(ctr, pos, rid, step), k0, k1);
     }
+    __device__ __forceinline__ uint4 block(uint32_t ctr) const { return ph(ctr); }
     // Gumbel-perturbed score z/T - log(-log u_i) of element i
     __device__ __forceinline__ float score(float v, int32_t ix, float invT) const
     {
@@ -453,13 +456,17 @@ __device__ __forceinline__ void score_vec(const float (&x)[VEC], float vm, int32
     const float D = ex2((vm * invT - best) * kLog2e);
     const float t = fmaf(-D, 16777216.f, 16777215.f) * 0.5f;
     const uint32_t kthr = (t >= 2.f) ? static_cast<uint32_t>(t) - 1u : 0u;
+    // (w >> 9) >= kthr  <=>  w >= kthr << 9 (kthr < 2^23); one test of the
+    // block's largest word passes over the usual block with nothing to score
+    const uint32_t wthr = kthr << 9;
 #pragma unroll
     for (int h = 0; h < VEC / 4; ++h) {
         const uint4 w = nz.block((static_cast<uint32_t>(base) >> 2) + h);
+        if (max(max(w.x, w.y), max(w.z, w.w)) < wthr) continue;
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if ((ws[j] >> 9) >= kthr)
+            if (ws[j] >= wthr)
                 keep_best(fmaf(x[4 * h + j], invT, gumbel_of(ws[j])), base + 4 * h + j, best, bi);
     }
 }
@@ -596,49 +603,6 @@ __device__ __forceinline__ ChunkGeom chunk_geom(const void *row, int c, int V)
 }
 
 // ------------------------------------------------------ stream kernel ----
-
-// The k-th largest of the CTA's thread maxima (k <= kThreads): at least k
-// distinct elements of the chunk are >= it.  The maxima's order-preserving
-// keys go to shared memory; warp 0 holds eight each and searches bit by bit
-// below the bits the smallest and largest share, keeping a bit when at least
-// k keys reach the prefix with it set (a warp sum per bit, no CTA barrier).
-template <typename E>
-__device__ __forceinline__ float kth_thread_max(float v, int k, float m_c, Shared &sh)
-{
-    constexpr int VS = (E::BYTES == 2) ? 16 : 0;
-    (void)m_c;
-    const int lane = threadIdx.x & 31;
-    sh.hist[threadIdx.x] = fkey(v) >> VS;
-    csync();
-    if (threadIdx.x < 32) {
-        uint32_t kv[kThreads / 32];
-        uint32_t mn = 0xFFFFFFFFu, mx = 0u;
-#pragma unroll
-        for (int j = 0; j < kThreads / 32; ++j) {
-            kv[j] = sh.hist[lane + 32 * j];
-            mn = min(mn, kv[j]);
-            mx = max(mx, kv[j]);
-        }
-        mn = __reduce_min_sync(0xFFFFFFFFu, mn);
-        mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-        const uint32_t x = mn ^ mx;
-        const int top = x ? 31 - __clz(x) : -1;
-        // every key lies in [mn, mx]: the bits above `top` are theirs
-        uint32_t ans = (top >= 31) ? 0u : (mx >> (top + 1)) << (top + 1);
-        for (int bit = top; bit >= 0; --bit) {
-            const uint32_t cand = ans | (1u << bit);
-            uint32_t c = 0;
-#pragma unroll
-            for (int j = 0; j < kThreads / 32; ++j) c += (kv[j] >= cand) ? 1u : 0u;
-            if (__reduce_add_sync(0xFFFFFFFFu, c) >= static_cast<uint32_t>(k)) ans = cand;
-        }
-        if (lane == 0) sh.sel_excl_u = ans;
-    }
-    csync();
-    const uint32_t ans = sh.sel_excl_u;
-    const uint32_t key = VS ? ((ans << 16) | ((ans & 0x8000u) ? 0u : 0xFFFFu)) : ans;
-    return key_floor(key);
-}
 
 // CTA reduction of the per-thread (max, first argmax, sum exp(z - max),
 // count) into the chunk summary sh.part: the maximum first, then the lowest

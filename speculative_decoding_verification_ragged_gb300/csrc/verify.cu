@@ -209,14 +209,20 @@ __device__ void summary_top_p_bf16(const VerifyParams &p, const uint4 *body, con
             const float D = ex2((vm * f.invT - s_top) * kLog2e);
             const float t = fmaf(-D, 16777216.f, 16777215.f) * 0.5f;
             const uint32_t kthr = (t >= 2.f) ? static_cast<uint32_t>(t) - 1u : 0u;
+            const uint32_t wthr = kthr << 9;      // (w >> 9) >= kthr <=> w >= kthr << 9
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+                // a Philox block whose four elements all lie below the
+                // counted range lists nothing: its noise is not drawn
+                const float bm = fmaxf(fmaxf(x[4 * h], x[4 * h + 1]), fmaxf(x[4 * h + 2], x[4 * h + 3]));
+                if (!(bm >= zbot)) continue;
                 const uint4 w = nz.block((static_cast<uint32_t>(base) >> 2) + h);
+                if (max(max(w.x, w.y), max(w.z, w.w)) < wthr) continue;
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float xv = x[4 * h + j];
-                    if (xv >= zbot && (ws[j] >> 9) >= kthr)
+                    if (xv >= zbot && ws[j] >= wthr)
                         list(xv, base + 4 * h + j, fmaf(xv, f.invT, gumbel_of(ws[j])));
                 }
             }
@@ -325,6 +331,9 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
 
     const int tid = threadIdx.x;
     const int nchunk = p.nchunk;
+    // the finish kernel's CTAs may become resident once every CTA of this
+    // grid has started (they wait for its completion before reading)
+    griddep_launch_dependents();
     // The sampler takes chunk-major order: a chunk's cost depends on its
     // row's filters, and this spreads every row's chunks evenly over the
     // grid, with the short tail chunks in the last wave.  Uniform modes keep
@@ -586,8 +595,9 @@ __device__ __forceinline__ void stage_maxima(const VerifyParams &p, int r, float
 // thread t) whose recorded maximum (staged in mxs) reaches L contributes that
 // maximum from its record; the few slots whose second largest element
 // reaches L as well are collected into a flat list in shared memory and read
-// back whole, one 16-byte vector per thread at a time, so their loads go out
-// in one batch.  Head / tail elements of a slot come with its first vector.
+// back whole, four 16-byte vectors per thread loaded before any is used, so
+// their loads go out in one batch.  Head / tail elements of a slot come with
+// its first vector.
 template <typename E, typename TIn>
 __device__ void gather_above(const VerifyParams &p, int r, const TIn *row, float L, const float *mxs,
                              Cand *lst, int cap, int *slots, int slot_cap, Shared &sh)
@@ -604,21 +614,36 @@ __device__ void gather_above(const VerifyParams &p, int r, const TIn *row, float
     };
     // a slot whose maximum reaches L gives that maximum (value and offset
     // are recorded); only a slot whose second largest element reaches L too
-    // is read back whole
+    // is read back whole.  The records of eight chunks are loaded together
+    // before any is used, so their loads go out in one batch.
     const float *mxr = reinterpret_cast<const float *>(reinterpret_cast<const Cand *>(p.ws_cand) +
                                                        static_cast<int64_t>(r) * nchunk * kCandCap);
     constexpr int CE = kChunkBytes / E::BYTES;
-    for (int q = 0; q < nchunk; ++q) {
-        const float m = mxs[q * kThreads + tid];
-        if (!(m >= L)) continue;
-        const float *area = mxr + static_cast<int64_t>(q) * kMaxStride;
-        const float sv = __ldcg(area + kThreads + tid);
-        const uint16_t a = __ldcg(reinterpret_cast<const unsigned short *>(area + 2 * kThreads) + tid);
-        if (sv >= L) {
-            const int k = warp_append(&sh.total);
-            if (k < slot_cap) slots[k] = q * kThreads + tid;
-        } else {
-            add(m, q * CE + static_cast<int32_t>(a));
+    for (int q0 = 0; q0 < nchunk; q0 += 8) {
+        float m[8], sv[8];
+        uint16_t a[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int q = q0 + u;
+            m[u] = (q < nchunk) ? mxs[q * kThreads + tid] : -INFINITY;
+            sv[u] = -INFINITY;
+            a[u] = 0;
+            if (m[u] >= L) {
+                const float *area = mxr + static_cast<int64_t>(q) * kMaxStride;
+                sv[u] = __ldcg(area + kThreads + tid);
+                a[u] = __ldcg(reinterpret_cast<const unsigned short *>(area + 2 * kThreads) + tid);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (!(m[u] >= L)) continue;
+            const int q = q0 + u;
+            if (sv[u] >= L) {
+                const int k = warp_append(&sh.total);
+                if (k < slot_cap) slots[k] = q * kThreads + tid;
+            } else {
+                add(m[u], q * CE + static_cast<int32_t>(a[u]));
+            }
         }
     }
     csync();
@@ -628,24 +653,39 @@ __device__ void gather_above(const VerifyParams &p, int r, const TIn *row, float
         csync();
         return;
     }
-    for (int e = tid; e < ns * PER; e += kThreads) {
-        const int sl = slots[e / PER], j = e - (e / PER) * PER;
-        const int q = sl / kThreads, t = sl - q * kThreads;
-        const ChunkGeom g = chunk_geom<E>(row, q, p.V);
-        const int i = t + j * kThreads;
-        if (i < g.nb) {
-            const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(row + g.a0) + i);
-            if (E::vmax(v) >= L) {
-                float x[VEC];
-                E::unpack(v, x);
-                for (int u = 0; u < VEC; ++u)
-                    if (x[u] >= L) add(x[u], g.a0 + i * VEC + u);
+    // the listed slots' vectors, four per thread loaded before any is used
+    for (int e0 = 0; e0 < ns * PER; e0 += 4 * kThreads) {
+        uint4 v[4];
+        int32_t ix0[4], ixe[4];
+        float xe[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * kThreads + tid;
+            ix0[u] = -1;
+            ixe[u] = -1;
+            if (e < ns * PER) {
+                const int sl = slots[e / PER], j = e - (e / PER) * PER;
+                const int q = sl / kThreads, t = sl - q * kThreads;
+                const ChunkGeom g = chunk_geom<E>(row, q, p.V);
+                const int i = t + j * kThreads;
+                if (i < g.nb) {
+                    v[u] = __ldcg(reinterpret_cast<const uint4 *>(row + g.a0) + i);
+                    ix0[u] = g.a0 + i * VEC;
+                }
+                if (j == 0 && t < g.n_extra) {
+                    ixe[u] = (t < g.n_head) ? g.e0 + t : g.a1 + (t - g.n_head);
+                    xe[u] = E::load(row, ixe[u]);
+                }
             }
         }
-        if (j == 0 && t < g.n_extra) {
-            const int32_t ix = (t < g.n_head) ? g.e0 + t : g.a1 + (t - g.n_head);
-            const float xv = E::load(row, ix);
-            if (xv >= L) add(xv, ix);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (ixe[u] >= 0 && xe[u] >= L) add(xe[u], ixe[u]);
+            if (ix0[u] < 0 || !(E::vmax(v[u]) >= L)) continue;
+            float x[VEC];
+            E::unpack(v[u], x);
+            for (int w = 0; w < VEC; ++w)
+                if (x[w] >= L) add(x[w], ix0[u] + w);
         }
     }
     csync();
@@ -675,7 +715,7 @@ __device__ float kth_maximum(const VerifyParams &p, const float *mxs, int k, flo
 // One CTA per packed row, after the stream kernel: combine the chunk
 // summaries, pick the row's token, write the row results, run the chain.
 template <typename TIn, int MODE>
-__global__ void __launch_bounds__(kThreads) finish_rows_kernel(const VerifyParams p)
+__global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyParams p)
 {
     using E = Elt<TIn>;
     extern __shared__ __align__(128) uint8_t smem[];

@@ -80,21 +80,92 @@ def assert_requests_equal(got: dict, ref, mask=None):
     np.testing.assert_array_equal(got["next_token"][sel], ref.next_token[sel])
 
 
-# a sampled token may differ from the fp64 definition only where a float
-# threshold decision or the Gumbel winner is within rounding of a tie
-FILTER_MARGIN = 1e-4
-GUMBEL_MARGIN = 1e-4
+# ---------------------------------------------------------------------------
+# Sampled tokens.  The kernels take the filter decisions and the Gumbel
+# argmax in fp32; the oracle takes them in fp64.  A row may come out
+# differently only where one of those decisions lies within the fp32 error
+# of its boundary.  The bands below bound that error per row, from the
+# operations the kernels perform (U = 2^-24, the fp32 unit roundoff):
+#
+#   min-p   th = M + T*logf(min_p): logf within 1 ulp (2U), the product and
+#           the sum rounded once each, so |th - th_exact| <= T|ln min_p| 3U
+#           + |th| U.  In ratio space (the oracle's margin is the relative
+#           distance of exp((z - M)/T) from min_p) that is at most
+#           (|ln min_p| 3U + |th| U / T), with 1% slack for exp(x) - 1 > x.
+#   top-p   every weight exp((z - M)/T) is ex2.approx (relative error below
+#           4U) of an argument (z - M) * log2(e)/T carrying 3U relative
+#           (1/T, log2(e)/T and the product rounded) plus |M| log2(e)/T U
+#           when M is folded into an fma constant; the sums add at most
+#           kSumDepth terms in sequence.  With A = the mass-weighted mean of
+#           |z - M| log2(e)/T over the row, every partial mass is within
+#           e_w = ln2 U (3A + |M| log2(e)/T) + 4U + kSumDepth U of exact, and
+#           the decision "mass above < top_p W" can flip only if the
+#           oracle's margin |above - top_p W| / W is below 2 e_w.
+#   Gumbel  score = z * (1/T) + g(u): the product carries 2U |z/T|, the sum
+#           U |score|, the noise g = -log(-log u) an absolute error below
+#           2^-20 (hardware log2, within 2^-22 absolute / relative).  Two
+#           scores can swap only if their fp64 gap is below
+#           2 (3U S + 2^-20), S = max|z|/T + 17.
+U32 = 2.0 ** -24
+kSumDepth = 64      # longest run of sequential fp32 additions of a mass
 
 
-def compare_sampled(vb, got: dict, ref, max_frac: float = 1e-4):
+def sample_bands(vb, p, rows_T=None):
+    """Per packed row: (filter band, Gumbel band) inside which an fp32
+    implementation may decide differently from the fp64 definition."""
+    R = vb.R
+    owner = np.repeat(np.arange(vb.B), np.diff(vb.cu_rows))[:R]
+    T = p.temperature.astype(np.float64)[owner]
+    tp = p.top_p.astype(np.float64)[owner]
+    mp = p.min_p.astype(np.float64)[owner]
+    z = vb.logits[:R, :vb.V]
+    z = W.bf16_bits_to_f32(z) if vb.dtype == "bf16" else z
+    z = z.astype(np.float64)
+    band_f = np.zeros(R)
+    band_g = np.zeros(R)
+    for r in range(R):
+        if not T[r] > 0:
+            continue
+        zr = z[r]
+        M = zr.max()
+        if not np.isfinite(M):
+            continue
+        sc = np.log2(np.e) / T[r]
+        bf = 0.0
+        if mp[r] > 0:
+            th = M + T[r] * np.log(mp[r])
+            bf = max(bf, 1.01 * (abs(np.log(mp[r])) * 3 * U32 + abs(th) * U32 / T[r]))
+        if tp[r] < 1:
+            arg = (zr - M) * sc
+            w = np.exp2(arg)
+            A = float((w * np.abs(arg)).sum() / w.sum())
+            e_w = np.log(2) * U32 * (3 * A + abs(M) * sc) + 4 * U32 + kSumDepth * U32
+            bf = max(bf, 2 * e_w)
+        band_f[r] = bf
+        S = np.abs(zr[np.isfinite(zr)]).max() / T[r] + 17.0
+        band_g[r] = 2 * (3 * U32 * S + 2.0 ** -20)
+    return band_f, band_g
+
+
+def compare_sampled(vb, p, got: dict, ref, max_frac: float = 1e-4, label: str = ""):
+    """Row tokens against the oracle.  A row may differ only inside its
+    bands (sample_bands); at most floor(max_frac * R) rows may differ at
+    all.  Prints the count of differing rows and of rows whose decisions lie
+    inside a band, and returns the number of differing rows."""
     R = vb.R
     g = got["row_token"][:R]
     o = ref.rows["row_token"]
-    near = (ref.rows["margin_filter"] < FILTER_MARGIN) | (ref.rows["margin_gumbel"] < GUMBEL_MARGIN)
+    band_f, band_g = sample_bands(vb, p)
+    near_f = ref.rows["margin_filter"] < band_f
+    near_g = ref.rows["margin_gumbel"] < band_g
     bad = (g != o)
-    assert not (bad & ~near).any(), (
-        "sampled tokens differ away from float ties at rows %s" % np.nonzero(bad & ~near)[0][:10])
-    assert bad.sum() <= max(1, int(max_frac * R)), "too many boundary disagreements: %d" % bad.sum()
+    print("sampled-token check %s: %d rows, %d differ (%d differ inside a filter band, %d inside "
+          "a Gumbel band); %d / %d rows have a decision inside a band"
+          % (label, R, bad.sum(), (bad & near_f).sum(), (bad & near_g & ~near_f).sum(),
+             near_f.sum(), near_g.sum()))
+    assert not (bad & ~(near_f | near_g)).any(), (
+        "sampled tokens differ away from float ties at rows %s" % np.nonzero(bad & ~(near_f | near_g))[0][:10])
+    assert bad.sum() <= int(max_frac * R), "too many boundary disagreements: %d" % bad.sum()
     # requests whose rows all agree must agree exactly
     ok_req = np.array([not bad[vb.cu_rows[b]:vb.cu_rows[b + 1]].any() for b in range(vb.B)])
     assert_requests_equal(got, ref, ok_req)

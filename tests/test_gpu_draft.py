@@ -19,9 +19,50 @@ def run_conf(sv, db, selected=None, threshold=0.3, max_rows=0, x=None):
                                     threshold=threshold, max_rows=max_rows))
 
 
-def check_alloc(got, ref, B, k):
-    near = ref.margin < 1e-5      # a threshold or budget decision at a float tie
-    if not near:
+U32 = 2.0 ** -24
+
+
+def near_requests(ref, B, k, threshold, max_rows):
+    """Requests whose allocation may legitimately differ from the oracle's.
+    Every confidence is checked within CONF_RTOL, so the cumulative product
+    c_bj of j + 1 of them is within (j + 1) CONF_RTOL + j U of exact (1%
+    slack for the compounding).  A threshold decision can flip only where
+    |c_bj - threshold| / threshold is below that; a budget cut only where
+    the relative gap between the last kept and the first dropped c is below
+    twice it (then both of their requests are excused)."""
+    cum = np.cumprod(ref.conf.reshape(B, k).astype(np.float64), axis=1)
+    band = 1.01 * (np.arange(1, k + 1) * CONF_RTOL + np.arange(k) * U32)
+    near = np.zeros(B, bool)
+    if threshold > 0:
+        near |= (np.abs(cum - threshold) / threshold < band[None, :]).any(axis=1)
+    want = (cum >= threshold).sum(axis=1)
+    if max_rows > 0 and want.sum() + B > max_rows >= B:
+        e = sorted(((cum[b, j], b, j) for b in range(B) for j in range(want[b])),
+                   key=lambda x: (-x[0], x[1], x[2]))
+        keep = max_rows - B
+        if 0 < keep < len(e) and e[keep - 1][0] > 0:
+            if (e[keep - 1][0] - e[keep][0]) / e[keep - 1][0] < 2 * band[-1]:
+                near[e[keep - 1][1]] = near[e[keep][1]] = True
+    return near
+
+
+def check_alloc(got, ref, B, k, threshold, max_rows, expect_no_tie=False):
+    """Allocations request by request: every request outside a float tie
+    gets the oracle's k_alloc and the oracle's packed rows (drafts, owner,
+    position) at its own offset; with no tie at all the whole layout agrees."""
+    near = near_requests(ref, B, k, threshold, max_rows)
+    print("allocation check: %d requests, %d inside a tie band" % (B, near.sum()))
+    if expect_no_tie:
+        assert not near.any(), "the fixed-seed workload has a decision inside a tie band"
+    cu, rcu = got["cu_rows"], ref.cu_rows
+    for b in np.nonzero(~near)[0]:
+        assert got["k_alloc"][b] == ref.k_alloc[b], "request %d" % b
+        g = slice(cu[b], cu[b + 1])
+        o = slice(rcu[b], rcu[b + 1])
+        np.testing.assert_array_equal(got["packed_draft"][g], ref.packed_draft[o], err_msg="request %d" % b)
+        np.testing.assert_array_equal(got["row_owner"][g], ref.row_owner[o], err_msg="request %d" % b)
+        np.testing.assert_array_equal(got["row_pos"][g], ref.row_pos[o], err_msg="request %d" % b)
+    if not near.any():
         np.testing.assert_array_equal(got["k_alloc"], ref.k_alloc)
         np.testing.assert_array_equal(got["cu_rows"], ref.cu_rows)
         np.testing.assert_array_equal(got["row_owner"], ref.row_owner)
@@ -29,9 +70,9 @@ def check_alloc(got, ref, B, k):
         np.testing.assert_array_equal(got["packed_draft"], ref.packed_draft)
         assert got["total_rows"][0] == ref.total_rows
     # structural invariants always hold
-    cu = got["cu_rows"]
     assert cu[0] == 0 and (np.diff(cu) == got["k_alloc"] + 1).all()
     assert (got["row_owner"][cu[-1]:] == -1).all()
+    return near
 
 
 @pytest.mark.parametrize("planted", [False, True])
@@ -45,7 +86,7 @@ def test_mtp_confidence_workload(planted, dtype):
     np.testing.assert_allclose(got["conf"], ref.conf, rtol=CONF_RTOL, atol=0)
     vals = W.bf16_bits_to_f32(db.draft_logits) if dtype == "bf16" else db.draft_logits
     np.testing.assert_array_equal(got["draft_token"], np.argmax(vals[:, :db.V], axis=1))
-    check_alloc(got, ref, db.B, db.k)
+    check_alloc(got, ref, db.B, db.k, 0.3, 0, expect_no_tie=True)
     assert got["status"][0] == 0
 
 
@@ -57,7 +98,7 @@ def test_budgeted_allocation(G):
                                   max_rows=G)
     got = run_conf(sv, db, threshold=0.05, max_rows=G)
     np.testing.assert_allclose(got["conf"], ref.conf, rtol=CONF_RTOL, atol=0)
-    check_alloc(got, ref, db.B, db.k)
+    check_alloc(got, ref, db.B, db.k, 0.05, G)
     assert got["total_rows"][0] <= max(G, db.B)
 
 
@@ -71,7 +112,7 @@ def test_selected_tokens_and_bad_selection():
     got = run_conf(sv, db, selected=sel, threshold=0.0)
     np.testing.assert_allclose(got["conf"], ref.conf, rtol=CONF_RTOL, atol=1e-30)
     assert got["status"][0] == ref.status == 0x20
-    check_alloc(got, ref, db.B, db.k)
+    check_alloc(got, ref, db.B, db.k, 0.0, 0)
 
 
 def test_budget_below_batch_is_reported():
@@ -81,7 +122,7 @@ def test_budget_below_batch_is_reported():
                                   max_rows=5)
     got = run_conf(sv, db, threshold=0.0, max_rows=5)
     assert got["status"][0] == ref.status == 0x80
-    check_alloc(got, ref, db.B, db.k)
+    check_alloc(got, ref, db.B, db.k, 0.0, 5)
 
 
 def test_adaptive_verify_pipeline_on_device():
@@ -99,7 +140,10 @@ def test_adaptive_verify_pipeline_on_device():
     ref_a = oracle.draft_confidence(db.draft_logits, "bf16", db.V, db.B, db.k, threshold=0.3)
     ref = oracle.verify_greedy(db.target_logits, "bf16", db.V, db.B, db.k, ref_a.cu_rows,
                                ref_a.packed_draft)
-    if ref_a.margin >= 1e-5:
-        np.testing.assert_array_equal(got["out_tokens"], ref.out_tokens)
-        np.testing.assert_array_equal(got["accepted_len"], ref.accepted_len)
+    # the target rows are indexed by packed row, so the two sides see the
+    # same rows only with the same layout: the fixed seed has no tie
+    check_alloc(a, ref_a, db.B, db.k, 0.3, 0, expect_no_tie=True)
+    np.testing.assert_array_equal(got["out_tokens"], ref.out_tokens)
+    np.testing.assert_array_equal(got["accepted_len"], ref.accepted_len)
+    np.testing.assert_array_equal(got["next_token"], ref.next_token)
     assert (got["accepted_len"] <= a["k_alloc"]).all()

@@ -114,7 +114,8 @@ def test_relaxed_topk_ragged(dtype):
 
 def test_relaxed_eagle_workload_with_fused_stats():
     """EAGLE-relaxed: B=256, k=5, V=152064 bf16, planted peaks, K=4; counters
-    accumulated over several steps by the fused path and by spec_prefix_stats."""
+    accumulated over 20 seeded steps by the fused path and by
+    spec_prefix_stats, every step's requests compared with the oracle."""
     sv = need_gpu()
     dev = "cuda"
     acc = torch.zeros(5, dtype=torch.int64, device=dev)
@@ -122,8 +123,8 @@ def test_relaxed_eagle_workload_with_fused_stats():
     hist = torch.zeros(6, dtype=torch.int64, device=dev)
     acc2, ver2, hist2 = acc.clone(), ver.clone(), hist.clone()
     racc = rver = rhist = None
-    for step in range(3):
-        vb = W.relaxed_planted(seed=W.data_seed(5, step))
+    steps = 0
+    for vb in W.relaxed_steps(20):
         K = vb.extra["relaxed_k"]
         ref = oracle.verify_relaxed(vb.logits, vb.dtype, vb.V, vb.B, vb.k_max, vb.cu_rows,
                                     vb.draft_ids, K)
@@ -134,10 +135,13 @@ def test_relaxed_eagle_workload_with_fused_stats():
         assert_requests_equal(got, ref)
         racc, rver, rhist, _ = oracle.prefix_stats(ref.accepted_len, vb.cu_rows, vb.B, vb.k_max,
                                                    racc, rver, rhist)
+        steps += 1
+    assert steps == 20
     torch.cuda.synchronize()
     for a, b in [(acc, racc), (ver, rver), (hist, rhist), (acc2, racc), (ver2, rver),
                  (hist2, rhist)]:
         np.testing.assert_array_equal(a.cpu().numpy(), b)
+    assert rver[0] == 20 * 256 and rhist.sum() == 20 * 256
 
 
 @pytest.mark.parametrize("dtype,V,ld", [("bf16", 50_000, 50_003), ("f32", 33_001, 33_001),

@@ -3,8 +3,11 @@ Gumbel-max sampling with Philox4x32-10 uniforms per row and the point-mass
 rejection chain per request, against the CPU oracle.
 
 Sampled tokens must match the fp64 definition on every row except where the
-oracle reports a float tie (a min-p / top-p decision or the Gumbel winner
-within 1e-4 of its boundary); at most 1 row in 10^4 may take that allowance.
+oracle reports a decision (a min-p / top-p threshold or the Gumbel winner)
+within the fp32 error band of its boundary (tests/_gpu.py derives the bands
+per row); at most floor(10^-4 R) rows of a batch may take that allowance,
+which is none below 10^4 rows.  The full-size workload must agree on every
+row.
 """
 import numpy as np
 import pytest
@@ -16,12 +19,13 @@ from tests._gpu import compare_sampled, host, need_gpu, run_sample, t, torch
 pytestmark = pytest.mark.gpu
 
 
-def check(sv, vb, p, **kw):
+def check(sv, vb, p, label="", **kw):
     ref = oracle.verify_sample(vb.logits, vb.dtype, vb.V, vb.B, vb.k_max, vb.cu_rows,
                                vb.draft_ids, p)
     got = host(run_sample(sv, vb, p, rows=True, **kw))
-    compare_sampled(vb, got, ref)
+    n_bad = compare_sampled(vb, p, got, ref, label=label)
     assert got["status"][0] == ref.status
+    got["n_differ"] = n_bad
     return got, ref
 
 
@@ -38,7 +42,8 @@ def test_stochastic_full_size_workload():
     launch configuration -- every row compared."""
     sv = need_gpu()
     vb, p = W.stochastic()
-    check(sv, vb, p)
+    got, _ = check(sv, vb, p, label="full-size workload")
+    assert got["n_differ"] == 0
 
 
 @pytest.mark.parametrize("T,k,tp,mp", [

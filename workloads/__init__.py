@@ -319,6 +319,58 @@ def relaxed_planted(seed: int = data_seed(5), B: int = 256, k: int = 5, V: int =
     return vb
 
 
+def relaxed_steps(n_steps: int = 20, seed: int = data_seed(5), B: int = 256, k: int = 5,
+                  V: int = QWEN_VOCAB, sigma: float = 3.0, gap: float = 8.0,
+                  p_planted: float = 0.7, p_near: float = 0.5, relaxed_k: int = 4):
+    """Seeded steps of the EAGLE-relaxed workload (bf16), one VerifyBatch per
+    step.  The N(0, sigma) rows are drawn once (seed); step s (its own
+    generator, seeded by (seed, s)) permutes them, plants a peak per row at
+    (largest other value) + gap and draws the drafts as relaxed_planted
+    does, from the row's planted token, its 2nd..4th largest tokens or a
+    uniform token.  Each step costs a copy instead of a fresh draw of
+    R x V normals."""
+    R = B * (k + 1)
+    base = _normal_rows(np.random.default_rng(seed), R, V, sigma)
+    # per base row: largest and second largest fp32 value (the planted value
+    # is the largest *other* value + gap) and the five largest bf16 values'
+    # tokens, by value then index (the near drafts after planting)
+    part = np.argpartition(-base[:, :V], 1, axis=1)[:, :2]
+    pv = np.take_along_axis(base, part, axis=1)
+    first = np.where(pv[:, 0] >= pv[:, 1], 0, 1)
+    top_tok = part[np.arange(R), first]
+    top1 = pv[np.arange(R), first]
+    top2 = pv[np.arange(R), 1 - first]
+    enc = _encode(base, "bf16")
+    vals = bf16_bits_to_f32(enc)
+    p5 = np.argpartition(-vals[:, :V], 5, axis=1)[:, :5]
+    key = np.take_along_axis(vals, p5, axis=1)
+    o5 = np.lexsort((p5, -key), axis=1)
+    top5 = np.take_along_axis(p5, o5, axis=1)
+    del vals
+    cu = _uniform_cu_rows(B, k)
+    rows = np.arange(R)
+    for s in range(n_steps):
+        rng = np.random.default_rng([seed, s])
+        perm = rng.permutation(R)
+        e = enc[perm]
+        tok = rng.integers(0, V, size=R).astype(np.int32)
+        other = np.where(tok == top_tok[perm], top2[perm], top1[perm])
+        e[rows, tok] = bf16_bits((other + np.float32(gap)).astype(np.float32)[:, None])[:, 0]
+        # ranks 2..4 after planting: the base row's largest tokens other than tok
+        cand = top5[perm]
+        keep = cand != tok[:, None]
+        ranked = np.array([c[m][:3] for c, m in zip(cand, keep)])
+        near = ranked[rows, rng.integers(0, 3, size=R)]
+        rand = rng.integers(0, V, size=R)
+        u = rng.random(R)
+        prop = np.where(u < p_planted, tok,
+                        np.where(rng.random(R) < p_near, near, rand)).astype(np.int32)
+        vb = VerifyBatch(e, "bf16", V, B, k, cu, _drafts_from(cu, prop))
+        vb.extra["relaxed_k"] = np.full(B, relaxed_k, dtype=np.int32)
+        vb.extra["planted"] = tok
+        yield vb
+
+
 def ragged_batch(seed: int, B: int, k_max: int, V: int, dtype: str = "bf16",
                  sigma: float = 3.0, p_top: float = 0.6, ld: Optional[int] = None,
                  k_values: Optional[np.ndarray] = None, plant_gap: Optional[float] = None,
