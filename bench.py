@@ -318,7 +318,8 @@ def run_ours(args) -> None:
         }
         if entries is not None:
             for e in entries.values():
-                e["pct_of_peak"] = round(100 * e["hbm_gbs"] / peaks["hbm_gbs"], 1)
+                if "hbm_gbs" in e:
+                    e["pct_of_peak"] = round(100 * e["hbm_gbs"] / peaks["hbm_gbs"], 1)
             line["entry_points"] = entries
             if entry_errors:
                 line["entry_point_errors"] = entry_errors

@@ -46,19 +46,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // try_wait that lets the hardware suspend the thread for up to `ns`
 // nanoseconds while the phase is incomplete (no busy polling)
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns)
@@ -150,14 +137,6 @@ __device__ __forceinline__ float warp_max_f32(float v)
     return r;
 }
 
-// Minimum of a float over the full warp (NaN operands ignored, as fminf).
-__device__ __forceinline__ float warp_min_f32(float v)
-{
-    float r;
-    asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
-}
-
 __device__ __forceinline__ float ex2(float x)
 {
     float y;
@@ -198,21 +177,6 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
 {
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// a + b rounded toward -inf in each half
-__device__ __forceinline__ uint64_t f2_add_rm(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
 

@@ -358,64 +358,6 @@ __device__ __forceinline__ void block_best(float &best, int32_t &bi, Shared &sh)
     csync();
 }
 
-// block minimum and maximum of a key (result in every thread)
-__device__ __forceinline__ void block_minmax(uint32_t &mn, uint32_t &mx, Shared &sh)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, o));
-        mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-    }
-    if ((threadIdx.x & 31) == 0) {
-        sh.red_i[threadIdx.x >> 5] = static_cast<int32_t>(mn);
-        sh.red_i[kWarps + (threadIdx.x >> 5)] = static_cast<int32_t>(mx);
-    }
-    csync();
-    mn = 0xFFFFFFFFu;
-    mx = 0u;
-    for (int q = 0; q < kWarps; ++q) {
-        mn = min(mn, static_cast<uint32_t>(sh.red_i[q]));
-        mx = max(mx, static_cast<uint32_t>(sh.red_i[kWarps + q]));
-    }
-    csync();
-}
-
-// Top-k bound inside a chunk for k above the thread count: the highest level
-// L = m_c - D (D from a fixed ladder) with at least k thread maxima >= L.
-// Thread maxima are distinct elements, so at least k elements of the chunk
-// are >= L and the chunk's share of the row's top k lies above it.  False
-// if no level qualifies.
-__device__ __forceinline__ bool kth_level(float thread_max, float m_c, int k, float &level,
-                                          Shared &sh)
-{
-    constexpr int NL = 8;
-    const float ladder[NL] = {0.25f, 0.5f, 1.f, 2.f, 3.f, 4.f, 6.f, 8.f};
-    int cnt[NL];
-#pragma unroll
-    for (int l = 0; l < NL; ++l) cnt[l] = (thread_max >= m_c - ladder[l]) ? 1 : 0;
-#pragma unroll
-    for (int l = 0; l < NL; ++l) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cnt[l] += __shfl_xor_sync(0xFFFFFFFFu, cnt[l], o);
-    }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int *wc = reinterpret_cast<int *>(sh.hist);        // [kWarps][NL]
-    if (lane == 0)
-#pragma unroll
-        for (int l = 0; l < NL; ++l) wc[warp * NL + l] = cnt[l];
-    csync();
-    int sel = -1;
-    for (int l = 0; l < NL; ++l) {
-        int t = 0;
-        for (int w = 0; w < kWarps; ++w) t += wc[w * NL + l];
-        if (t >= k) { sel = l; break; }
-    }
-    csync();
-    if (sel < 0) return false;
-    level = m_c - ladder[sel];
-    return true;
-}
-
 // Philox4x32-10 stream of one row: counter (i >> 2, position, request id,
 // step), key (seed lo, seed hi); element i takes word i & 3.
 struct Noise {
