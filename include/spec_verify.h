@@ -315,9 +315,12 @@ typedef struct {
  * (a prefix, since c is non-increasing).  With max_rows = G > 0 and
  * sum(k_b + 1) > G, only the best G - B positions are kept, ordered by
  * (c desc, b asc, j asc).  Then cu_rows = exclusive scan of (k_b + 1) and the
- * per-row owner / position / draft token of the packed layout.  Two kernel
- * launches; nothing is read back to the host.  The workspace comes from
- * spec_draft_workspace_bytes.
+ * per-row owner / position / draft token of the packed layout.  Three kernel
+ * launches (the draft rows' streaming pass, the per-row finish, the
+ * allocation), the last two chained by programmatic dependent launch;
+ * nothing is read back to the host.  The workspace comes from
+ * spec_draft_workspace_bytes.  A batch with 8 B k + 16 B + 4 bytes above
+ * 200 KiB (the allocation stages it on chip) returns SPEC_ERR_UNSUPPORTED.
  */
 SPEC_API int spec_draft_confidence(const spec_draft *draft, const spec_allocation *out,
                                    void *workspace, size_t workspace_bytes, spec_stream stream);

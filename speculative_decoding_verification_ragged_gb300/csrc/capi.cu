@@ -297,7 +297,7 @@ int spec_draft_confidence(const spec_draft *d, const spec_allocation *o, void *w
     if (reinterpret_cast<uintptr_t>(d->draft_logits) % elt_bytes(d->dtype)) return SPEC_ERR_INVALID_ARG;
     if (static_cast<size_t>(d->V) * elt_bytes(d->dtype) > max_row_bytes()) return SPEC_ERR_UNSUPPORTED;
     const int64_t Q = static_cast<int64_t>(d->B) * d->k;
-    if (Q * 4 + (static_cast<int64_t>(d->B) * 4 + 1) * 4 > 200 * 1024) return SPEC_ERR_UNSUPPORTED;
+    if (Q * 8 + (static_cast<int64_t>(d->B) * 4 + 1) * 4 > 200 * 1024) return SPEC_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(Q) * d->ld > (int64_t(1) << 40)) return SPEC_ERR_UNSUPPORTED;
     if (Q * chunks_per_row(d->V, static_cast<int>(elt_bytes(d->dtype))) > INT32_MAX)
         return SPEC_ERR_UNSUPPORTED;

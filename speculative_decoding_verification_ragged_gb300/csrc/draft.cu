@@ -12,7 +12,7 @@
 
 namespace specv {
 
-constexpr int kAllocThreads = 1024;
+constexpr int kAllocThreads = 256;
 
 // block-wide sum of an int64 over kAllocThreads threads
 __device__ long long block_sum(long long v, long long *scratch)
@@ -60,9 +60,13 @@ __device__ int block_exclusive_scan(int *v, int n, int *scratch)
 __global__ void __launch_bounds__(kAllocThreads) alloc_kernel(const AllocParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
+    // launched while the confidence kernels run: their results are complete
+    // and visible past this wait
+    griddep_wait();
     const int B = p.B, k = p.k, Q = B * k;
     float *cum = reinterpret_cast<float *>(smem_raw);        // [Q]
-    int *ka = reinterpret_cast<int *>(cum + Q);              // [B]
+    int *tok = reinterpret_cast<int *>(cum + Q);             // [Q]
+    int *ka = tok + Q;                                       // [B]
     int *gt = ka + B;                                        // [B]
     int *eq = gt + B;                                        // [B]
     int *cu = eq + B;                                        // [B+1]
@@ -70,12 +74,19 @@ __global__ void __launch_bounds__(kAllocThreads) alloc_kernel(const AllocParams 
     __shared__ int iscr[kAllocThreads / 32];
     const int tid = threadIdx.x;
 
+    // the confidences and draft tokens staged in shared memory, every load
+    // in flight at once
+    for (int q = tid; q < Q; q += kAllocThreads) {
+        cum[q] = p.conf[q];
+        tok[q] = p.draft_token[q];
+    }
+    __syncthreads();
     // cumulative confidence per request (in order, fp32) and threshold count
     for (int b = tid; b < B; b += kAllocThreads) {
         float c = 1.f;
         int cnt = 0;
         for (int j = 0; j < k; ++j) {
-            c *= p.conf[b * k + j];
+            c *= cum[b * k + j];
             cum[b * k + j] = c;
             cnt += (c >= p.threshold) ? 1 : 0;
         }
@@ -155,7 +166,7 @@ __global__ void __launch_bounds__(kAllocThreads) alloc_kernel(const AllocParams 
             const int r = cu[b] + j;
             p.row_owner[r] = b;
             p.row_pos[r] = j;
-            if (p.packed_draft) p.packed_draft[r] = (j < ka[b]) ? p.draft_token[b * k + j] : -1;
+            if (p.packed_draft) p.packed_draft[r] = (j < ka[b]) ? tok[b * k + j] : -1;
         }
     }
     if (tid == 0) {
@@ -166,13 +177,33 @@ __global__ void __launch_bounds__(kAllocThreads) alloc_kernel(const AllocParams 
 
 cudaError_t launch_alloc(const AllocParams &p, cudaStream_t stream)
 {
-    const size_t smem = static_cast<size_t>(p.B) * p.k * sizeof(float) +
+    const size_t smem = static_cast<size_t>(p.B) * p.k * (sizeof(float) + sizeof(int)) +
                         (static_cast<size_t>(p.B) * 4 + 1) * sizeof(int);
-    cudaError_t e = cudaFuncSetAttribute(alloc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    // the shared-memory limit is raised once per device (to the most any
+    // accepted batch needs: the entry point bounds it by 200 KiB)
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    alloc_kernel<<<1, kAllocThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(alloc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    // programmatic dependent launch after the confidence kernels (the
+    // kernel waits for them before reading)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(kAllocThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, alloc_kernel, p);
 }
 
 // ------------------------------------------ compact rows to request slots --

@@ -893,7 +893,8 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
             const int32_t s = p.selected ? __ldg(p.selected + r) : AMAX;
             float cf = 0.f;
             if (s >= 0 && s < p.V) {
-                const float zs = E::load(row, s);
+                // the argmax's own logit is the row maximum: no load
+                const float zs = p.selected ? E::load(row, s) : M;
                 cf = (S > 0.f) ? ex2((zs - M) * kLog2e) / S : 0.f;
             } else {
                 set_status(p.status, SPEC_STATUS_BAD_SELECTED);
