@@ -100,6 +100,21 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// The same copy with an L2 eviction-first hint: for data read exactly once
+// (the logits), so that it does not push out the small per-chunk summaries
+// the next kernel reads back.
+__device__ __forceinline__ void bulk_g2s_stream(void *dst, const void *src, uint32_t bytes,
+                                                uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], pol;\n\t}"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Barrier of the CTA's compute warps only (named barrier 2, kThreads
 // threads): the ticket warp of the row kernel never joins it.
 __device__ __forceinline__ void csync()

@@ -87,12 +87,49 @@ static_assert(kFrontCap * sizeof(Front) + kTopBins * sizeof(uint16_t) <= kCandCa
               "listed elements and counts fit a chunk's candidate area");
 static_assert(kThreads * (2 * sizeof(float) + sizeof(uint16_t)) <= kCandCap * sizeof(Cand),
               "thread maxima, second values and offsets fit");
-constexpr int kMaxStride = kCandCap * static_cast<int>(sizeof(Cand) / sizeof(float));  // floats per chunk area
 // the finish stages gathered candidates, then the survivors' tallies
 static_assert(kListCap * sizeof(Cand) + kTally * (sizeof(uint32_t) + sizeof(uint64_t)) <= kFinScratch,
               "gathered candidates and tallies fit the finish scratch");
 // bf16 top-p alone stages every chunk's counts (longer rows take the exact path)
 constexpr int kCountChunks = static_cast<int>(kFinScratch / (kTopBins * sizeof(uint16_t)));
+
+// Record of a top-k / min-p (and fp32 top-p alone) chunk, at the start of
+// its candidate area: per thread slot its maximum, its second largest
+// element (both in the input type: bf16 bits for bf16 rows) and the
+// maximum's offset in the chunk.  The finish copies every chunk's record of
+// its row into shared memory with one bulk copy each.
+template <typename E>
+struct Rec {
+    static constexpr int BYTES = kThreads * (2 * E::BYTES + 2);
+    static __device__ __forceinline__ float max(const uint8_t *r, int t) { return val(r, t); }
+    static __device__ __forceinline__ float sec(const uint8_t *r, int t) { return val(r, kThreads + t); }
+    static __device__ __forceinline__ uint16_t off(const uint8_t *r, int t)
+    {
+        return reinterpret_cast<const uint16_t *>(r + 2 * kThreads * E::BYTES)[t];
+    }
+    static __device__ __forceinline__ void put(uint8_t *r, int t, float mx, float sc, uint16_t o)
+    {
+        if constexpr (E::BYTES == 2) {
+            reinterpret_cast<uint16_t *>(r)[t] = static_cast<uint16_t>(__float_as_uint(mx) >> 16);
+            reinterpret_cast<uint16_t *>(r)[kThreads + t] = static_cast<uint16_t>(__float_as_uint(sc) >> 16);
+        } else {
+            reinterpret_cast<float *>(r)[t] = mx;
+            reinterpret_cast<float *>(r)[kThreads + t] = sc;
+        }
+        reinterpret_cast<uint16_t *>(r + 2 * kThreads * E::BYTES)[t] = o;
+    }
+  private:
+    static __device__ __forceinline__ float val(const uint8_t *r, int i)
+    {
+        if constexpr (E::BYTES == 2)
+            return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(r)[i]) << 16);
+        else
+            return reinterpret_cast<const float *>(r)[i];
+    }
+};
+static_assert(Rec<Elt<float>>::BYTES <= kCandCap * sizeof(Cand), "a record fits a chunk's candidate area");
+static_assert(Rec<Elt<uint16_t>>::BYTES % 16 == 0 && Rec<Elt<float>>::BYTES % 16 == 0,
+              "records are whole 16-byte units (bulk copies)");
 
 // ---------------------------------------------------------- prologue -----
 // One warp per packed row: its row record (row_record); extra CTAs handle
@@ -302,11 +339,8 @@ __device__ void summary_sampler(const VerifyParams &p, const RowInfo &info, cons
     // of the chunk, extras included) its maximum, its second largest element
     // and the maximum's offset in the chunk; for fp32 top-p alone also the
     // chunk's mass at temperature T
-    float *mx = reinterpret_cast<float *>(reinterpret_cast<Cand *>(p.ws_cand) + rc * kCandCap);
-    mx[tid] = thread_max;
-    mx[kThreads + tid] = thread_sec;
-    reinterpret_cast<uint16_t *>(mx + 2 * kThreads)[tid] =
-        static_cast<uint16_t>(thread_max > -INFINITY ? thread_arg - g.e0 : 0);
+    Rec<E>::put(reinterpret_cast<uint8_t *>(reinterpret_cast<Cand *>(p.ws_cand) + rc * kCandCap), tid,
+                thread_max, thread_sec, static_cast<uint16_t>(thread_max > -INFINITY ? thread_arg - g.e0 : 0));
     if (f.pure_p && m_c > -INFINITY) {
         float mass = (T != 1.0f) ? chunk_mass<E>(body, g.nb, m_c, f.sc) : 0.f;
         if (T != 1.0f && tid < g.n_extra) mass += ex2((sh.extras_v[tid] - m_c) * f.sc);
@@ -363,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
         fence_mbar_init();
         const uint32_t bytes = static_cast<uint32_t>(g.nb) * 16u;
         mbar_arrive_expect_tx(&sh.mbar[0], bytes + (HAS_INFO ? 64u : 0u));
-        if (bytes) bulk_g2s(smem, row + g.a0, bytes, &sh.mbar[0]);
+        if (bytes) bulk_g2s_stream(smem, row + g.a0, bytes, &sh.mbar[0]);
         int32_t R = p.n_rows;
         if (MODE != MODE_CONF) R = __ldg(p.cu_rows + p.B);
         if (HAS_INFO) {
@@ -570,36 +604,16 @@ __device__ bool finish_top_p_bf16(const VerifyParams &p, const RowInfo &info, co
     return true;
 }
 
-// The row's thread maxima (nchunk x kThreads floats, chunk-major) staged in
-// shared memory with one batch of loads per thread.
-__device__ __forceinline__ void stage_maxima(const VerifyParams &p, int r, float *mxs)
-{
-    const int tid = threadIdx.x;
-    const int nchunk = p.nchunk;
-    const float *mxr = reinterpret_cast<const float *>(reinterpret_cast<const Cand *>(p.ws_cand) +
-                                                       static_cast<int64_t>(r) * nchunk * kCandCap);
-    for (int q0 = 0; q0 < nchunk; q0 += 8) {
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            if (q0 + u < nchunk) v[u] = __ldcg(mxr + static_cast<int64_t>(q0 + u) * kMaxStride + tid);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            if (q0 + u < nchunk) mxs[(q0 + u) * kThreads + tid] = v[u];
-    }
-    csync();
-}
-
 // Every element of row r with a value at or above L, into lst (count in
 // sh.cand_n; above cap the list is incomplete).  A thread slot (chunk q,
-// thread t) whose recorded maximum (staged in mxs) reaches L contributes that
-// maximum from its record; the few slots whose second largest element
+// thread t) whose maximum (from the records staged in recs) reaches L
+// contributes that maximum; the few slots whose second largest element
 // reaches L as well are collected into a flat list in shared memory and read
 // back whole, four 16-byte vectors per thread loaded before any is used, so
 // their loads go out in one batch.  Head / tail elements of a slot come with
 // its first vector.
 template <typename E, typename TIn>
-__device__ void gather_above(const VerifyParams &p, int r, const TIn *row, float L, const float *mxs,
+__device__ void gather_above(const VerifyParams &p, const TIn *row, float L, const uint8_t *recs,
                              Cand *lst, int cap, int *slots, int slot_cap, Shared &sh)
 {
     constexpr int VEC = E::VEC;
@@ -612,38 +626,16 @@ __device__ void gather_above(const VerifyParams &p, int r, const TIn *row, float
         const int slot = warp_append(&sh.cand_n);
         if (slot < cap) { lst[slot].v = v; lst[slot].i = ix; }
     };
-    // a slot whose maximum reaches L gives that maximum (value and offset
-    // are recorded); only a slot whose second largest element reaches L too
-    // is read back whole.  The records of eight chunks are loaded together
-    // before any is used, so their loads go out in one batch.
-    const float *mxr = reinterpret_cast<const float *>(reinterpret_cast<const Cand *>(p.ws_cand) +
-                                                       static_cast<int64_t>(r) * nchunk * kCandCap);
     constexpr int CE = kChunkBytes / E::BYTES;
-    for (int q0 = 0; q0 < nchunk; q0 += 8) {
-        float m[8], sv[8];
-        uint16_t a[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int q = q0 + u;
-            m[u] = (q < nchunk) ? mxs[q * kThreads + tid] : -INFINITY;
-            sv[u] = -INFINITY;
-            a[u] = 0;
-            if (m[u] >= L) {
-                const float *area = mxr + static_cast<int64_t>(q) * kMaxStride;
-                sv[u] = __ldcg(area + kThreads + tid);
-                a[u] = __ldcg(reinterpret_cast<const unsigned short *>(area + 2 * kThreads) + tid);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (!(m[u] >= L)) continue;
-            const int q = q0 + u;
-            if (sv[u] >= L) {
-                const int k = warp_append(&sh.total);
-                if (k < slot_cap) slots[k] = q * kThreads + tid;
-            } else {
-                add(m[u], q * CE + static_cast<int32_t>(a[u]));
-            }
+    for (int q = 0; q < nchunk; ++q) {
+        const uint8_t *rq = recs + q * Rec<E>::BYTES;
+        const float m = Rec<E>::max(rq, tid);
+        if (!(m >= L)) continue;
+        if (Rec<E>::sec(rq, tid) >= L) {
+            const int k = warp_append(&sh.total);
+            if (k < slot_cap) slots[k] = q * kThreads + tid;
+        } else {
+            add(m, q * CE + static_cast<int32_t>(Rec<E>::off(rq, tid)));
         }
     }
     csync();
@@ -691,17 +683,17 @@ __device__ void gather_above(const VerifyParams &p, int r, const TIn *row, float
     csync();
 }
 
-// The k-th largest of the row's thread maxima (counting equal ones; staged
-// in mxs): at least k elements of the row reach it, so the row's top k
-// values lie at or above it.
+// The k-th largest of the row's thread maxima (counting equal ones; from
+// the records staged in recs): at least k elements of the row reach it, so
+// the row's top k values lie at or above it.
 template <typename E>
-__device__ float kth_maximum(const VerifyParams &p, const float *mxs, int k, float M, Shared &sh)
+__device__ float kth_maximum(const VerifyParams &p, const uint8_t *recs, int k, float M, Shared &sh)
 {
     const int nchunk = p.nchunk;
     if (k > nchunk * kThreads) return -INFINITY;
     auto visit = [&](auto &&fn, float thr) {
         for (int q = 0; q < nchunk; ++q) {
-            const float v = mxs[q * kThreads + threadIdx.x];
+            const float v = Rec<E>::max(recs + q * Rec<E>::BYTES, threadIdx.x);
             if (v >= thr) fn(v, 0);
         }
     };
@@ -723,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
     ChunkPart *parts = reinterpret_cast<ChunkPart *>(smem + sizeof(Shared));     // [kMaxChunks]
     uint8_t *scratch = reinterpret_cast<uint8_t *>(parts + kMaxChunks);          // [kFinScratch]
     Cand *lst = reinterpret_cast<Cand *>(scratch);                              // [kListCap]
-    float *mxs = reinterpret_cast<float *>(scratch + kFinScratch);              // [kMaxChunks * kThreads]
+    uint8_t *recs = scratch + kFinScratch;                      // sampler: [nchunk] chunk records
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = blockIdx.x;
     const int nchunk = p.nchunk;
@@ -745,6 +737,17 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
         mbar_init(&sh.mbar[0], 1);
         mbar_init(&sh.mbar[1], 1);
         fence_mbar_init();
+        if (MODE == MODE_SAMPLE) {
+            // every chunk's record, whatever the row's filters (it is not
+            // known yet): the copies run with the loads below, and a
+            // top-k / min-p row finds its records on chip
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(
+                reinterpret_cast<const Cand *>(p.ws_cand) + static_cast<int64_t>(r) * nchunk * kCandCap);
+            mbar_arrive_expect_tx(&sh.mbar[0], static_cast<uint32_t>(nchunk * Rec<E>::BYTES));
+            for (int q = 0; q < nchunk; ++q)
+                bulk_g2s(recs + q * Rec<E>::BYTES, src + static_cast<int64_t>(q) * kCandCap * sizeof(Cand),
+                         Rec<E>::BYTES, &sh.mbar[0]);
+        }
     }
     if (tid < nchunk) {
         const ChunkPart *rp = reinterpret_cast<const ChunkPart *>(p.ws_part) + static_cast<int64_t>(r) * nchunk;
@@ -754,6 +757,13 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
         cp.m = a.x; cp.amax = __float_as_int(a.y); cp.s = a.z; cp.aux = __float_as_int(a.w);
         cp.g = b.x; cp.w = b.y; cp.ncand = __float_as_int(b.z); cp.lev = b.w;
         parts[tid] = cp;
+    }
+    if (MODE == MODE_SAMPLE && tid == 0 && !mbar_wait(&sh.mbar[0], 0)) {
+        // the records did not land in time: reported; one more bounded wait
+        // for the copies, and the row is not settled from them
+        set_status(p.status, SPEC_STATUS_TIMEOUT);
+        mbar_wait(&sh.mbar[0], 0);
+        sh.timeout = 1;
     }
     csync();
     const RowInfo &info = sh.info;
@@ -818,15 +828,14 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
             const float th_m = f.use_m ? M + T * logf(info.min_p) : -INFINITY;
             float L = th_m;
             const int kk = f.use_k ? info.top_k : (f.pure_p ? kPureListK : 0);
-            stage_maxima(p, r, mxs);
-            if (kk > 0) L = fmaxf(L, kth_maximum<E>(p, mxs, kk, M, sh));
+            if (kk > 0) L = fmaxf(L, kth_maximum<E>(p, recs, kk, M, sh));
             // the gathered slots' list shares the scratch with the
             // candidates: slots from the top, candidates from the bottom
             constexpr int kSlotCap = 1024;
             static_assert(kListCap * sizeof(Cand) + kSlotCap * sizeof(int) <= kFinScratch, "slots fit");
-            gather_above<E, TIn>(p, r, row, L, mxs, lst, kListCap,
+            gather_above<E, TIn>(p, row, L, recs, lst, kListCap,
                                  reinterpret_cast<int *>(scratch + kFinScratch) - kSlotCap, kSlotCap, sh);
-            const int n_list = sh.cand_n;
+            const int n_list = sh.timeout ? kListCap + 1 : sh.cand_n;
             auto visit_lst = [&](auto &&fn, float thr) {
                 for (int i = tid; i < n_list; i += kThreads) {
                     const Cand e = lst[i];
@@ -993,12 +1002,12 @@ template <typename TIn, int MODE>
 static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
 {
     const size_t smem = kChunkBytes + sizeof(Shared);
-    // the finish stages the thread maxima of the row's nchunk chunks after
-    // its scratch (sampler only)
+    // the sampler's finish stages the records of the row's nchunk chunks
+    // after its scratch
     const size_t smem_fin_max = sizeof(Shared) + kMaxChunks * sizeof(ChunkPart) + kFinScratch +
-                                static_cast<size_t>(kMaxChunks) * kThreads * sizeof(float);
+                                (MODE == MODE_SAMPLE ? static_cast<size_t>(kMaxChunks) * Rec<Elt<TIn>>::BYTES : 0);
     const size_t smem_fin = sizeof(Shared) + kMaxChunks * sizeof(ChunkPart) + kFinScratch +
-                            (MODE == MODE_SAMPLE ? static_cast<size_t>(p.nchunk) * kThreads * sizeof(float) : 0);
+                            (MODE == MODE_SAMPLE ? static_cast<size_t>(p.nchunk) * Rec<Elt<TIn>>::BYTES : 0);
     const size_t smem_exact = sizeof(Shared) + 2 * kRowStage;
     auto kstream = stream_chunks_kernel<TIn, MODE>;
     auto kfin = finish_rows_kernel<TIn, MODE>;
