@@ -4,7 +4,8 @@
 // top-K acceptance; the filtered Gumbel-max sampler with the point-mass
 // rejection chain; and the draft confidence.
 //
-// Three kernels per call, chained with programmatic dependent launch:
+// Three kernels per call (four for the sampler), chained with programmatic
+// dependent launch:
 //
 //   prologue, one warp per packed row: the owner request (32-way search of
 //     cu_rows), the row's position and validity and the owner's parameters,
@@ -28,33 +29,37 @@
 //                     a lower bound from the thread maxima are skipped, and so
 //                     are the logarithms of elements whose uniform cannot
 //                     reach the running best);
-//       top-k/min-p - nothing but the 256 thread maxima: the survivors form
-//                     an upper set {z >= th}, and the finish bounds th from
-//                     below with them (at least k thread maxima, hence k
-//                     elements, reach the k-th largest maximum) and reads
-//                     back only the thread slices whose maximum reaches the
-//                     bound;
+//       top-k/min-p - a record of the 256 thread slices: each one's maximum,
+//                     second largest element and the maximum's offset (bf16
+//                     values as 16 bits); the survivors form an upper set
+//                     {z >= th}, and the finish bounds th from below with the
+//                     maxima (at least k thread maxima, hence k elements,
+//                     reach the k-th largest maximum) and reads back only the
+//                     slices whose second largest element reaches the bound;
 //       top-p alone - bf16: counts of the kTopBins bf16 values at and below
 //                     the chunk maximum, the chunk's mass at temperature T,
 //                     and the elements whose Gumbel score reaches that of the
-//                     chunk's first maximum; fp32: the thread maxima and the
+//                     chunk's first maximum; fp32: the record above and the
 //                     chunk's mass.
+//     The logits are copied with an L2 evict-first hint: they are read once,
+//     and the summaries the finish reads back stay in L2.
 //     Only plain stores: nothing in this kernel waits for another CTA.
 //
 //   finish, one CTA per row: combine the chunk summaries and settle the
 //     row's token: the best chunk score (no filter); a scan of the merged
 //     value counts from the top value to the nucleus boundary, then the best
 //     score at or above it (bf16 top-p alone); or, for top-k / min-p (and
-//     fp32 top-p alone), the elements at or above the bound gathered from
-//     the logits, radix selects over them (exact k-th largest value, exact
-//     top-p crossing by mass, or per-value tallies for a narrow bf16 set)
-//     and Gumbel-max over the survivors.  A row the summaries cannot settle
-//     (a nucleus reaching below every chunk's counted values, a list
-//     overflow) is sampled with exact selects over the whole row, streamed
-//     again.  The CTA finishing the last row of a request (atomic ticket)
-//     runs the accept-while-equal prefix scan with one warp ballot and
-//     writes the request's tokens and the optional prefix-acceptance
-//     counters.
+//     fp32 top-p alone), the row's chunk records bulk-copied on chip with
+//     its first loads, the elements at or above the bound gathered from them
+//     (and from the few slices read back), radix selects over them (exact
+//     k-th largest value, exact top-p crossing by mass, or per-value tallies
+//     for a narrow bf16 set) and Gumbel-max over the survivors.  A row the
+//     summaries cannot settle (a nucleus reaching below every chunk's
+//     counted values, a list overflow) is queued for the exact kernel: exact
+//     selects over the whole row, streamed again.  The CTA finishing the
+//     last row of a request (atomic ticket) runs the accept-while-equal
+//     prefix scan with one warp ballot and writes the request's tokens and
+//     the optional prefix-acceptance counters.
 //
 // Definitions: xLLM docs "自适应投机推理" §"启动示例" (ragged rejection
 // sampler with packed-row owners, point-mass draft, replacement / bonus,
@@ -82,7 +87,7 @@ struct __align__(8) Front {
 };
 static_assert(kChunkBytes / 2 <= 65536, "a bf16 chunk offset fits 16 bits");
 // a chunk's candidate area holds its listed elements then its value counts
-// (bf16 top-p alone), or its thread maxima (other filtered rows)
+// (bf16 top-p alone), or its record (other filtered rows)
 static_assert(kFrontCap * sizeof(Front) + kTopBins * sizeof(uint16_t) <= kCandCap * sizeof(Cand),
               "listed elements and counts fit a chunk's candidate area");
 static_assert(kThreads * (2 * sizeof(float) + sizeof(uint16_t)) <= kCandCap * sizeof(Cand),
