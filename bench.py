@@ -45,8 +45,9 @@ KERNEL_SOURCES = ["speculative_decoding_verification_ragged_gb300/csrc/verify.cu
                   "speculative_decoding_verification_ragged_gb300/csrc/common.cuh"]
 
 
-# kernels one spec_verify_sample call launches: prologue, stream, finish and
-# the exact-selects kernel (which leaves at once when no row needs it)
+# kernels one spec_verify_sample call launches: the row records, stream,
+# finish and the exact-selects kernel (which leaves at once when no row
+# needs it)
 LAUNCHES_PER_CALL = 4
 
 
@@ -303,7 +304,7 @@ def run_ours(args) -> None:
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "traffic": traffic_record(), "peak_source": peaks["source"],
-                         "kernel": "spec_verify_sample call (row_info + stream_chunks + "
+                         "kernel": "spec_verify_sample call (sample_records + stream_chunks + "
                                    "finish_rows + exact_rows kernels, bf16)",
                          "algorithmic_bytes_per_launch": bytes_per_launch,
                          "mean_launch_us": round(mean_launch_ms * 1e3, 3),

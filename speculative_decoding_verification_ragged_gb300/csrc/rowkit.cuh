@@ -29,7 +29,9 @@ constexpr float kMassTol = 1e-5f;       // relative slack of a mass that must ho
 // -log(-log u) <= 24 ln 2 = 16.636; the bound used leaves a margin.
 constexpr float kGumbelMax = 16.75f;
 
-// row record written by the prologue (64 bytes)
+// row record (64 bytes): computed by warp 0 of each stream CTA and stored
+// by the row's first chunk for the finish; for the sampler, written by the
+// records kernel before the stream kernel
 struct __align__(16) RowInfo {
     int32_t b, pos, k_b, valid;
     int32_t draft, K, top_k, bad;

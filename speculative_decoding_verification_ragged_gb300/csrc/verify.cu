@@ -4,22 +4,24 @@
 // top-K acceptance; the filtered Gumbel-max sampler with the point-mass
 // rejection chain; and the draft confidence.
 //
-// Three kernels per call (four for the sampler), chained with programmatic
+// Two kernels per call (four for the sampler), chained with programmatic
 // dependent launch:
 //
-//   prologue, one warp per packed row: the owner request (32-way search of
-//     cu_rows), the row's position and validity and the owner's parameters,
-//     as a 64-byte row record; requests without a valid row range get their
-//     outputs here.  With a confidence margin it also decides whether the
-//     margin applies to the row (position, generated-token count, a warp
-//     scan of the protected ids) and records the draft's logit (NaN if not).
+//   records (sampler only), one warp per packed row: the row record (see
+//     below), before the stream kernel; the exact kernel's queue is reset.
 //
 //   stream, one CTA per (row, chunk of kChunkBytes): thread 0 issues one 1-D
-//     TMA bulk copy of the chunk's 16-byte-aligned body into shared memory,
-//     then one of the row record on the same mbarrier once the prologue has
-//     finished (the row is read from HBM exactly once; unaligned head / tail
+//     TMA bulk copy of the chunk's 16-byte-aligned body into shared memory
+//     (the row is read from HBM exactly once; unaligned head / tail
 //     elements use plain loads); many short CTAs per SM keep the copies in
-//     flight and hide each other's latencies.  Pass 1 takes two loops over
+//     flight and hide each other's latencies.  While the copy is in flight,
+//     warp 0 computes the row record (the sampler copies it from the
+//     records kernel): the owner request (32-way search of
+//     cu_rows), the row's position and validity and the owner's parameters;
+//     with a confidence margin also whether the margin applies (position,
+//     generated-token count, a warp scan of the protected ids) and the
+//     draft's logit (NaN if not).  The row's first chunk stores the record
+//     for the finish.  Pass 1 takes two loops over
 //     the thread's 16-byte vectors: the maximum and the first vector holding
 //     it (selects only), then sum exp(z - max) against it (packed f32x2
 //     arithmetic for bf16) and, for relaxed top-K, the count of logits above
@@ -45,7 +47,8 @@
 //     and the summaries the finish reads back stay in L2.
 //     Only plain stores: nothing in this kernel waits for another CTA.
 //
-//   finish, one CTA per row: combine the chunk summaries and settle the
+//   finish, one CTA per row (extra CTAs write the outputs of requests
+//     without a valid row range): combine the chunk summaries and settle the
 //     row's token: the best chunk score (no filter); a scan of the merged
 //     value counts from the top value to the nucleus boundary, then the best
 //     score at or above it (bf16 top-p alone); or, for top-k / min-p (and
@@ -60,6 +63,9 @@
 //     last row of a request (atomic ticket) runs the accept-while-equal
 //     prefix scan with one warp ballot and writes the request's tokens and
 //     the optional prefix-acceptance counters.
+//
+//   exact (sampler only), 256 CTAs striding over the rows the finish
+//     queued; with an empty queue they leave at once.
 //
 // Definitions: xLLM docs "自适应投机推理" §"启动示例" (ragged rejection
 // sampler with packed-row owners, point-mass draft, replacement / bonus,
@@ -136,23 +142,22 @@ static_assert(Rec<Elt<float>>::BYTES <= kCandCap * sizeof(Cand), "a record fits 
 static_assert(Rec<Elt<uint16_t>>::BYTES % 16 == 0 && Rec<Elt<float>>::BYTES % 16 == 0,
               "records are whole 16-byte units (bulk copies)");
 
-// ---------------------------------------------------------- prologue -----
-// One warp per packed row: its row record (row_record); extra CTAs handle
-// the requests without a valid row range (bad_request_outputs).
-template <typename TIn, int MODE>
-__global__ void __launch_bounds__(256) row_info_kernel(const VerifyParams p, int row_blocks)
+// ------------------------------------------------ sampler prologue -----
+// Sampler only: one warp per packed row writes its row record (row_record)
+// before the stream kernel needs it; the exact kernel's queue starts empty.
+// (The other modes' stream CTAs compute their own record while their copy
+// is in flight: there it costs less than this launch and its wait, while
+// the sampler's record, with its parameter loads, costs its stream CTAs
+// more.)
+template <typename TIn>
+__global__ void __launch_bounds__(256) sample_records_kernel(const VerifyParams p)
 {
     griddep_launch_dependents();
-    // the sampler's queue of rows for exact selects starts empty (the
-    // previous call's kernels have completed before this one starts)
-    if (MODE == MODE_SAMPLE && blockIdx.x == 0 && threadIdx.x == 0) p.ws_queue[0].x = 0;
-    if (static_cast<int>(blockIdx.x) >= row_blocks) {
-        bad_request_outputs(p, (blockIdx.x - row_blocks) * 256 + threadIdx.x);
-        return;
-    }
+    // the previous call's kernels have completed before this one starts
+    if (blockIdx.x == 0 && threadIdx.x == 0) p.ws_queue[0].x = 0;
     const int r = (blockIdx.x * 256 + threadIdx.x) >> 5;
     if (r >= p.R_cap) return;
-    const RowInfo inf = row_record<TIn, MODE>(p, r);
+    const RowInfo inf = row_record<TIn, MODE_SAMPLE>(p, r);
     if ((threadIdx.x & 31) == 0) reinterpret_cast<RowInfo *>(p.ws_info)[r] = inf;
 }
 
@@ -401,19 +406,30 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
         mbar_init(&sh.mbar[0], 1);
         fence_mbar_init();
         const uint32_t bytes = static_cast<uint32_t>(g.nb) * 16u;
-        mbar_arrive_expect_tx(&sh.mbar[0], bytes + (HAS_INFO ? 64u : 0u));
+        mbar_arrive_expect_tx(&sh.mbar[0], bytes + (MODE == MODE_SAMPLE ? 64u : 0u));
+        // (with no body and no record the arrival alone completes the phase)
         if (bytes) bulk_g2s_stream(smem, row + g.a0, bytes, &sh.mbar[0]);
         int32_t R = p.n_rows;
         if (MODE != MODE_CONF) R = __ldg(p.cu_rows + p.B);
-        if (HAS_INFO) {
-            griddep_wait();                 // row records of the prologue
+        if (MODE == MODE_SAMPLE) {
+            griddep_wait();                 // the sampler's row records
             bulk_g2s(&sh.info, reinterpret_cast<const RowInfo *>(p.ws_info) + r, 64u, &sh.mbar[0]);
-        } else {
+        }
+        if (!HAS_INFO) {
             RowInfo inf = {};
             inf.b = r; inf.valid = 1;
             sh.info = inf;
         }
         sh.R = min(R, p.R_cap);
+    }
+    if (HAS_INFO && MODE != MODE_SAMPLE && tid < 32) {
+        // the row record (owner request, position, parameters) while the
+        // copy is in flight; the row's first chunk stores it for the finish
+        const RowInfo inf = row_record<TIn, MODE>(p, r);
+        if (tid == 0) {
+            sh.info = inf;
+            if (c == 0) reinterpret_cast<RowInfo *>(p.ws_info)[r] = inf;
+        }
     }
     float xe = -INFINITY;
     int32_t ie = INT_MAX;
@@ -726,6 +742,12 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
     const int nchunk = p.nchunk;
 
     griddep_launch_dependents();           // the exact kernel may wait for this one
+    if (MODE != MODE_CONF && r >= p.R_cap) {
+        // extra CTAs: the outputs of requests without a valid row range
+        // (nothing of the stream kernel is read)
+        bad_request_outputs(p, (r - p.R_cap) * kThreads + tid);
+        return;
+    }
     griddep_wait();                        // the stream kernel's stores are visible
     if (tid == 0) {
         sh.fin = 0;
@@ -1042,10 +1064,12 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
         done[dev] = true;
     }
     const int rows = (MODE == MODE_CONF) ? p.n_rows : p.R_cap;
-    if (MODE != MODE_CONF) {
-        const int row_blocks = static_cast<int>((static_cast<int64_t>(p.R_cap) * 32 + 255) / 256);
-        const int req_blocks = (p.B + 255) / 256;
-        row_info_kernel<TIn, MODE><<<row_blocks + req_blocks, 256, 0, stream>>>(p, row_blocks);
+    // the finish kernel's extra CTAs write the outputs of requests without a
+    // valid row range
+    const int req_blocks = (MODE == MODE_CONF) ? 0 : (p.B + kThreads - 1) / kThreads;
+    if (MODE == MODE_SAMPLE) {
+        sample_records_kernel<TIn><<<static_cast<unsigned>((static_cast<int64_t>(rows) * 32 + 255) / 256), 256, 0,
+                                     stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -1064,11 +1088,14 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = (MODE != MODE_CONF) ? 1 : 0;
+    // the first kernel of a call runs in plain stream order, after
+    // everything the caller queued before (the previous call included); the
+    // sampler's follows its records kernel
+    cfg.numAttrs = (MODE == MODE_SAMPLE) ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kstream, p);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cf = {};
-    cf.gridDim = dim3(static_cast<unsigned>(rows), 1, 1);
+    cf.gridDim = dim3(static_cast<unsigned>(rows + req_blocks), 1, 1);
     cf.blockDim = dim3(kThreads, 1, 1);
     cf.dynamicSmemBytes = smem_fin;
     cf.stream = stream;
