@@ -712,6 +712,27 @@ __device__ float kth_maximum(const VerifyParams &p, const uint8_t *recs, int k, 
 {
     const int nchunk = p.nchunk;
     if (k > nchunk * kThreads) return -INFINITY;
+    // one round over the 256 16-bit keys just below the row maximum's (bin
+    // = distance from it, so the maxima spread over the bins instead of
+    // piling into the one or two bins of a first radix digit): for bf16 the
+    // crossing bin is the exact key; for fp32 its 16-bit floor, a lower bound
+    // that serves as well
+    const uint32_t top = fkey(M) >> 16;
+    sh.hist[threadIdx.x] = 0u;
+    csync();
+    for (int q = 0; q < nchunk; ++q) {
+        const uint32_t d = top - (fkey(Rec<E>::max(recs + q * Rec<E>::BYTES, threadIdx.x)) >> 16);
+        if (d < 256u) atomicAdd(&sh.hist[255u - d], 1u);
+    }
+    csync();
+    find_crossing<uint32_t>(sh.hist, static_cast<uint32_t>(k), sh);
+    if (sh.sel_found) {
+        const uint32_t key16 = top - (255u - static_cast<uint32_t>(sh.sel_bin));
+        csync();
+        return key_floor(key16 << 16);
+    }
+    csync();
+    // the k-th largest lies further below: the general select
     auto visit = [&](auto &&fn, float thr) {
         for (int q = 0; q < nchunk; ++q) {
             const float v = Rec<E>::max(recs + q * Rec<E>::BYTES, threadIdx.x);
