@@ -824,23 +824,28 @@ __device__ bool tally_top_p(Visit &&visit, uint32_t klo, uint32_t ktop, float M,
 // over their survivors), from a candidate list that holds every element of
 // the row at or above a bound whose key is klist (visit_lst yields them): the
 // survivors of top-k and min-p are the upper set {z >= th_S} (th_S from the
-// min-p level and an exact k-th-value select over the list); top-p keeps the
+// min-p level and the exact k-th value of the list, given as key_k or
+// selected here); top-p keeps the
 // group where their mass, counted from the top, first reaches top_p times
 // their total (per-value tallies when the survivors span at most kTally
 // bf16 values, else an exact mass select); Gumbel-max over what is left.
 // cnt [kTally] and bst [kTally] are shared scratch.  Result in best / bi.
 template <typename E, typename Visit>
 __device__ void settle_from_list(Visit &&visit_lst, const RowInfo &info, const Filter &f, float M,
-                                 uint32_t klist, uint32_t *cnt, unsigned long long *bst,
+                                 uint32_t klist, uint32_t key_k, uint32_t *cnt, unsigned long long *bst,
                                  GumbelScorer &gs, float &best, int32_t &bi, Shared &sh)
 {
     const float sc = f.sc;
     const uint32_t keyM = fkey(M);
     const float th_m = f.use_m ? M + f.T * logf(info.min_p) : -INFINITY;
     uint32_t key_S = f.use_m ? fkey(th_m) : 0u;
+    // key_k: the k-th largest value's key when the caller already has it
+    // (0xFFFFFFFF: not known, select it)
     if (f.use_k)
-        key_S = max(key_S, select_key<E, false>(visit_lst, max(key_S, klist), keyM, 0.f,
-                                                static_cast<uint32_t>(info.top_k), M, sc, sh));
+        key_S = max(key_S, key_k != 0xFFFFFFFFu
+                               ? key_k
+                               : select_key<E, false>(visit_lst, max(key_S, klist), keyM, 0.f,
+                                                      static_cast<uint32_t>(info.top_k), M, sc, sh));
     if (E::BYTES == 2 && f.use_p) {
         // the survivors tallied per value when they span at most kTally
         // bf16 values

@@ -923,7 +923,27 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
             } else {
                 // ---- top-k and / or min-p (then top-p over the survivors) --
                 uint32_t *cnt = reinterpret_cast<uint32_t *>(lst + kListCap);
-                settle_from_list<E>(visit_lst, info, f, M, fkey(L), cnt,
+                // a short list gives its k-th largest value by rank counts, one
+                // entry per thread, with no radix rounds
+                uint32_t key_k = 0xFFFFFFFFu;
+                if (f.use_k && n_list <= kThreads) {
+                    if (tid == 0) sh.sel_excl_u = fkey(L);      // fewer than k listed: all survive
+                    csync();
+                    if (tid < n_list) {
+                        const float v = lst[tid].v;
+                        int gt = 0, ge = 0;
+                        for (int j = 0; j < n_list; ++j) {
+                            const float w = lst[j].v;
+                            gt += (w > v) ? 1 : 0;
+                            ge += (w >= v) ? 1 : 0;
+                        }
+                        if (gt < info.top_k && info.top_k <= ge) sh.sel_excl_u = fkey(v);
+                    }
+                    csync();
+                    key_k = sh.sel_excl_u;
+                    csync();
+                }
+                settle_from_list<E>(visit_lst, info, f, M, fkey(L), key_k, cnt,
                                     reinterpret_cast<unsigned long long *>(cnt + kTally), gs, best, bi, sh);
             }
         }
