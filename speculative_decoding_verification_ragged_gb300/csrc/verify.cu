@@ -142,7 +142,7 @@ static_assert(Rec<Elt<float>>::BYTES <= kCandCap * sizeof(Cand), "a record fits 
 static_assert(Rec<Elt<uint16_t>>::BYTES % 16 == 0 && Rec<Elt<float>>::BYTES % 16 == 0,
               "records are whole 16-byte units (bulk copies)");
 
-// ------------------------------------------------ sampler prologue -----
+// ------------------------------------------------- sampler records -----
 // Sampler only: one warp per packed row writes its row record (row_record)
 // before the stream kernel needs it; the exact kernel's queue starts empty.
 // (The other modes' stream CTAs compute their own record while their copy

@@ -49,7 +49,7 @@ def test_stochastic_full_size_workload():
 @pytest.mark.parametrize("T,k,tp,mp", [
     (1.0, 0, 1.0, 0.0),      # no filter: Gumbel over the whole vocabulary
     (0.5, 0, 1.0, 0.0),
-    (1.0, 0, 0.9, 0.0),      # pure top-p (bin bracket, band settled exactly)
+    (1.0, 0, 0.9, 0.0),      # pure top-p (merged per-value counts, listed elements)
     (0.5, 0, 0.9, 0.0),
     (0.7, 0, 0.5, 0.0),
     (1.0, 20, 1.0, 0.0),     # top-k: chunk lists above the k-th thread maximum
@@ -173,9 +173,9 @@ def shifted(vb, shift):
 
 @pytest.mark.parametrize("T,tp,sigma,shift", [
     (0.5, 0.9, 3.0, 0.0),     # small nucleus: settled from the candidate lists
-    (1.0, 0.9, 3.0, 0.0),     # diffuse nucleus: band from one pass over the row
+    (1.0, 0.9, 3.0, 0.0),     # diffuse nucleus: settled from the counted values
     (2.0, 0.7, 3.0, 0.0),
-    (1.0, 0.9, 0.3, 0.0),     # nearly flat rows: the band overflows, exact row selects
+    (1.0, 0.9, 0.3, 0.0),     # nearly flat rows: the lists overflow, exact row selects
     (1e-6, 0.9, 3.0, 20.0),   # grid origin beyond 2^21: exact row selects
     (1.0, 0.99, 3.0, -40.0),  # all logits negative
     (0.25, 0.5, 8.0, 0.0),    # nucleus of one or two values
@@ -200,8 +200,9 @@ def test_pure_top_p_rows_not_vector_aligned(dtype):
 
 
 def test_many_diffuse_rows():
-    """Every row's nucleus is diffuse, and the queued rows' chunks outnumber
-    the heavy kernel's CTAs: each CTA takes several chunks of several rows."""
+    """Every row's nucleus is diffuse (80 requests): most rows are settled
+    from the counted values, and any the finish queues are taken by the
+    exact kernel's CTAs striding over the queue."""
     sv = need_gpu()
     vb = W.ragged_batch(seed=47, B=80, k_max=4, V=152064, dtype="bf16")
     check(sv, vb, params(vb.B, 1.0, 0, 0.9, 0.0, seed=9))
