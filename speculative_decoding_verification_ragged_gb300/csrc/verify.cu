@@ -81,8 +81,15 @@ namespace specv {
 
 constexpr int kTopBins = 256;       // bf16 top-p alone: values counted at and below the chunk max
 constexpr int kFrontCap = 384;      // bf16 top-p alone: listed elements per chunk
+// bf16 top-p alone: Philox blocks a warp may queue (two per 16-byte vector
+// of its share of a chunk), and the stream kernel's queue area after Shared
+constexpr int kQueuePerWarp = 2 * (kChunkBytes / 16) / kWarps;
+constexpr int kQueueBytes = kWarps * kQueuePerWarp * static_cast<int>(sizeof(uint16_t));
 constexpr int kFinScratch = 20 * 1024;   // finish kernel: candidates or counts (6 CTAs per SM)
 constexpr int kExactCtas = 256;          // CTAs of the exact kernel (strided over its queue)
+
+static_assert(5 * (kChunkBytes + sizeof(Shared) + kQueueBytes + 1024) <= 228 * 1024,
+              "five bf16 sampler stream CTAs fit an SM's shared memory");
 
 // Element listed by a bf16 top-p-alone chunk: its Gumbel score reaches the
 // score of the chunk's first maximum.  8 bytes: the score, then the bf16
@@ -240,51 +247,81 @@ __device__ void summary_top_p_bf16(const VerifyParams &p, const uint4 *body, con
     auto count = [&](float v) {
         if (v >= zbot) atomicAdd(&tally[ktop - (fkey(v) >> 16)], 1u);
     };
-    const bool whole_blocks = (g.a0 & 3) == 0;
-    for (int i = tid; i < g.nb; i += kThreads) {
-        const uint4 v = body[i];
-        const float vm = E::vmax(v);
-        if (!(vm >= zbot)) continue;
-        float x[8];
-        E::unpack(v, x);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) count(x[q]);
-        // no element of the vector can reach s_top (the noise is bounded)
-        if (fmaf(vm, f.invT, kGumbelMax) < s_top) continue;
-        const int32_t base = g.a0 + i * 8;
-        if (whole_blocks) {
-            const float D = ex2((vm * f.invT - s_top) * kLog2e);
-            const float t = fmaf(-D, 16777216.f, 16777215.f) * 0.5f;
-            const uint32_t kthr = (t >= 2.f) ? static_cast<uint32_t>(t) - 1u : 0u;
-            const uint32_t wthr = kthr << 9;      // (w >> 9) >= kthr <=> w >= kthr << 9
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                // a Philox block whose four elements all lie below the
-                // counted range lists nothing: its noise is not drawn
-                const float bm = fmaxf(fmaxf(x[4 * h], x[4 * h + 1]), fmaxf(x[4 * h + 2], x[4 * h + 3]));
-                if (!(bm >= zbot)) continue;
-                const uint4 w = nz.block((static_cast<uint32_t>(base) >> 2) + h);
-                if (max(max(w.x, w.y), max(w.z, w.w)) < wthr) continue;
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float xv = x[4 * h + j];
-                    if (xv >= zbot && ws[j] >= wthr)
-                        list(xv, base + 4 * h + j, fmaf(xv, f.invT, gumbel_of(ws[j])));
-                }
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (x[q] >= zbot) list(x[q], base + q, nz.score(x[q], base + q, f.invT));
-        }
-    }
+    // the head and tail elements first (plain loads, staged by the kernel)
     if (tid < g.n_extra) {
         const float xv = sh.extras_v[tid];
         const int32_t ix = sh.extras_i[tid];
         if (f.T != 1.0f) mass += ex2((xv - m_c) * f.sc);
         count(xv);
         if (xv >= zbot) list(xv, ix, nz.score(xv, ix, f.invT));
+    }
+    if ((g.a0 & 3) == 0) {
+        // The body covers whole Philox blocks.  Pass A counts the values and
+        // queues, per warp, the blocks that may list an element: one in the
+        // counted range, and a block maximum that reaches s_top with the
+        // largest noise.  About a third of the blocks qualify, but some lane
+        // of a warp nearly always needs its block, so a lane-by-lane skip
+        // would draw every block; pass B draws only the queued ones, packed
+        // by ballots.
+        const int lane = tid & 31;
+        const unsigned lt = (1u << lane) - 1u;
+        uint16_t *wq = reinterpret_cast<uint16_t *>(&sh + 1) + (tid >> 5) * kQueuePerWarp;
+        int nq = 0;
+        for (int i0 = tid - lane; i0 < g.nb; i0 += kThreads) {
+            const int i = i0 + lane;
+            bool q0 = false, q1 = false;
+            if (i < g.nb) {
+                float x[8];
+                E::unpack(body[i], x);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) count(x[q]);
+                const float b0 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                const float b1 = fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]));
+                q0 = b0 >= zbot && !(fmaf(b0, f.invT, kGumbelMax) < s_top);
+                q1 = b1 >= zbot && !(fmaf(b1, f.invT, kGumbelMax) < s_top);
+            }
+            const unsigned m0 = __ballot_sync(0xFFFFFFFFu, q0), m1 = __ballot_sync(0xFFFFFFFFu, q1);
+            if (q0) wq[nq + __popc(m0 & lt)] = static_cast<uint16_t>(2 * i);
+            nq += __popc(m0);
+            if (q1) wq[nq + __popc(m1 & lt)] = static_cast<uint16_t>(2 * i + 1);
+            nq += __popc(m1);
+        }
+        __syncwarp();
+        const uint2 *halves = reinterpret_cast<const uint2 *>(body);
+        const uint32_t ctr0 = static_cast<uint32_t>(g.a0) >> 2;
+        for (int e = lane; e < nq; e += 32) {
+            const uint32_t blk = wq[e];
+            const uint2 u = halves[blk];
+            const float x[4] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y)};
+            const float bm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            const float D = ex2((bm * f.invT - s_top) * kLog2e);
+            const float t = fmaf(-D, 16777216.f, 16777215.f) * 0.5f;
+            const uint32_t kthr = (t >= 2.f) ? static_cast<uint32_t>(t) - 1u : 0u;
+            const uint32_t wthr = kthr << 9;      // (w >> 9) >= kthr <=> w >= kthr << 9
+            const uint4 w = nz.block(ctr0 + blk);
+            if (max(max(w.x, w.y), max(w.z, w.w)) < wthr) continue;
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            const int32_t base = g.a0 + 4 * static_cast<int32_t>(blk);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (x[j] >= zbot && ws[j] >= wthr) list(x[j], base + j, fmaf(x[j], f.invT, gumbel_of(ws[j])));
+        }
+    } else {
+        for (int i = tid; i < g.nb; i += kThreads) {
+            const uint4 v = body[i];
+            const float vm = E::vmax(v);
+            if (!(vm >= zbot)) continue;
+            float x[8];
+            E::unpack(v, x);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) count(x[q]);
+            // no element of the vector can reach s_top (the noise is bounded)
+            if (fmaf(vm, f.invT, kGumbelMax) < s_top) continue;
+            const int32_t base = g.a0 + i * 8;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (x[q] >= zbot) list(x[q], base + q, nz.score(x[q], base + q, f.invT));
+        }
     }
     if (f.T != 1.0f) mass = block_sum(mass, sh);
     else csync();
@@ -1069,7 +1106,7 @@ size_t max_row_bytes() { return static_cast<size_t>(kMaxChunks) * kChunkBytes; }
 template <typename TIn, int MODE>
 static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
 {
-    const size_t smem = kChunkBytes + sizeof(Shared);
+    const size_t smem = kChunkBytes + sizeof(Shared) + ((MODE == MODE_SAMPLE && sizeof(TIn) == 2) ? kQueueBytes : 0);
     // the sampler's finish stages the records of the row's nchunk chunks
     // after its scratch
     const size_t smem_fin_max = sizeof(Shared) + kMaxChunks * sizeof(ChunkPart) + kFinScratch +
