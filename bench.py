@@ -45,10 +45,9 @@ KERNEL_SOURCES = ["speculative_decoding_verification_ragged_gb300/csrc/verify.cu
                   "speculative_decoding_verification_ragged_gb300/csrc/common.cuh"]
 
 
-# kernels one spec_verify_sample call launches: the row records, stream,
-# finish and the exact-selects kernel (which leaves at once when no row
-# needs it)
-LAUNCHES_PER_CALL = 4
+# kernels one spec_verify_sample call launches: the row records, stream and
+# finish kernels
+LAUNCHES_PER_CALL = 3
 
 
 def _code_only(text: str) -> str:
@@ -305,7 +304,7 @@ def run_ours(args) -> None:
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "traffic": traffic_record(), "peak_source": peaks["source"],
                          "kernel": "spec_verify_sample call (sample_records + stream_chunks + "
-                                   "finish_rows + exact_rows kernels, bf16)",
+                                   "finish_rows kernels, bf16)",
                          "algorithmic_bytes_per_launch": bytes_per_launch,
                          "mean_launch_us": round(mean_launch_ms * 1e3, 3),
                          "launch_us_p10_median_p90": [

@@ -142,8 +142,7 @@ typedef struct {
  * Workspace for the verify calls: per-row and per-chunk scratch (a row is
  * processed as ceil(V * element bytes / 32 KiB) chunks) and per-request
  * tickets; for spec_verify_sample (sampling != 0) also the sampler's
- * per-chunk candidate lists and mass bins (4.5 KiB per chunk) and the queue
- * of rows that need a second pass over their logits.  Size from
+ * per-chunk candidate lists and mass bins (4.5 KiB per chunk).  Size from
  * spec_workspace_bytes(R_cap, B, V, dtype, sampling).  It must be
  * ZERO-FILLED once before its first use; every completed call leaves the
  * ticket words at zero again, so one zeroed workspace serves any number of

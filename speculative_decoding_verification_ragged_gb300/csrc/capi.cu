@@ -29,18 +29,17 @@ struct WsLayout {
     int32_t *tok, *flag;
     uint32_t *ticket, *rticket;
     void *info, *part, *cand;
-    int4 *queue;
 };
 
 // tok [R_cap] | flag [R_cap] | ticket [B] | rticket [R_cap] | info [R_cap * 64 B] |
-// part [R_cap * nchunk * 32 B] | cand, queue (sampler only); 256-byte aligned
+// part [R_cap * nchunk * 32 B] | cand (sampler only); 256-byte aligned
 size_t ws_bytes(int32_t R_cap, int32_t B, int32_t V, int elt, bool sampling)
 {
     const size_t R = static_cast<size_t>(R_cap);
     const size_t rc = R * static_cast<size_t>(chunks_per_row(V, elt));
     size_t n = 3 * align256(R * 4) + align256(static_cast<size_t>(B) * 4) + align256(R * 64) +
                align256(rc * 32);
-    if (sampling) n += align256(rc * kWsCandCap * 8) + align256((R + 1) * 16);
+    if (sampling) n += align256(rc * kWsCandCap * 8);
     return n;
 }
 
@@ -62,11 +61,7 @@ WsLayout ws_layout(void *ws, int32_t R_cap, int32_t B, int32_t V, int elt, bool 
     p += align256(R * 64);
     l.part = p;
     p += align256(rc * 32);
-    if (sampling) {
-        l.cand = p;
-        p += align256(rc * kWsCandCap * 8);
-        l.queue = reinterpret_cast<int4 *>(p);
-    }
+    if (sampling) l.cand = p;
     return l;
 }
 
@@ -123,7 +118,6 @@ VerifyParams base_params(const spec_batch *b, const spec_outputs *o, void *ws, b
     p.ws_info = l.info;
     p.ws_part = l.part;
     p.ws_cand = l.cand;
-    p.ws_queue = l.queue;
     p.nchunk = chunks_per_row(b->V, elt);
     p.n_rows = b->R_cap;
     return p;

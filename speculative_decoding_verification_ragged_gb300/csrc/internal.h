@@ -16,8 +16,6 @@ enum Mode : int { MODE_GREEDY = 0, MODE_RELAXED = 1, MODE_SAMPLE = 2, MODE_CONF 
 //   cand[r][c]  (kWsCandCap (value, index) pairs) candidate lists, or for
 //               bf16 top-p alone the listed elements and value counts
 //                                                             (sampler only)
-//   queue       (1 + R_cap entries of 16 bytes) rows left for exact selects
-//               over the whole row (count first)                 (sampler only)
 constexpr int kWsCandCap = 512;
 
 // Everything one verify launch needs (passed by value to the row kernel).
@@ -70,7 +68,6 @@ struct VerifyParams {
     void *ws_info;               // [R_cap] row records (64 bytes each)
     void *ws_part;               // [R_cap * nchunk] chunk partials (32 bytes each)
     void *ws_cand;               // [R_cap * nchunk * kWsCandCap] (value, index) pairs
-    int4 *ws_queue;              // [1 + R_cap] {row, max bits, argmax, 0}; .x of entry 0 = count
     int32_t nchunk;              // chunks per row
     int32_t n_rows;              // rows of the work (R_cap; draft rows for the confidence)
 };

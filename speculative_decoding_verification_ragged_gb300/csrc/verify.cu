@@ -4,11 +4,11 @@
 // top-K acceptance; the filtered Gumbel-max sampler with the point-mass
 // rejection chain; and the draft confidence.
 //
-// Two kernels per call (four for the sampler), chained with programmatic
+// Two kernels per call (three for the sampler), chained with programmatic
 // dependent launch:
 //
 //   records (sampler only), one warp per packed row: the row record (see
-//     below), before the stream kernel; the exact kernel's queue is reset.
+//     below), before the stream kernel.
 //
 //   stream, one CTA per (row, chunk of kChunkBytes): thread 0 issues one 1-D
 //     TMA bulk copy of the chunk's 16-byte-aligned body into shared memory
@@ -58,14 +58,11 @@
 //     k-th largest value, exact top-p crossing by mass, or per-value tallies
 //     for a narrow bf16 set) and Gumbel-max over the survivors.  A row the
 //     summaries cannot settle (a nucleus reaching below every chunk's
-//     counted values, a list overflow) is queued for the exact kernel: exact
-//     selects over the whole row, streamed again.  The CTA finishing the
-//     last row of a request (atomic ticket) runs the accept-while-equal
-//     prefix scan with one warp ballot and writes the request's tokens and
-//     the optional prefix-acceptance counters.
-//
-//   exact (sampler only), 256 CTAs striding over the rows the finish
-//     queued; with an empty queue they leave at once.
+//     counted values, a list overflow) takes exact selects over the whole
+//     row, streamed again through the same CTA's shared memory.  The CTA
+//     finishing the last row of a request (atomic ticket) runs the
+//     accept-while-equal prefix scan with one warp ballot and writes the
+//     request's tokens and the optional prefix-acceptance counters.
 //
 // Definitions: xLLM docs "自适应投机推理" §"启动示例" (ragged rejection
 // sampler with packed-row owners, point-mass draft, replacement / bonus,
@@ -75,6 +72,8 @@
 // acceptance with a strict prefix, no per-request host sync, the active
 // vocabulary with a full token-id map), §"启动" and §"通用参数" (the
 // confidence margin and its position, token-count and protected-id options).
+#include <algorithm>
+
 #include "rowkit.cuh"
 
 namespace specv {
@@ -86,7 +85,6 @@ constexpr int kFrontCap = 384;      // bf16 top-p alone: listed elements per chu
 constexpr int kQueuePerWarp = 2 * (kChunkBytes / 16) / kWarps;
 constexpr int kQueueBytes = kWarps * kQueuePerWarp * static_cast<int>(sizeof(uint16_t));
 constexpr int kFinScratch = 20 * 1024;   // finish kernel: candidates or counts (6 CTAs per SM)
-constexpr int kExactCtas = 256;          // CTAs of the exact kernel (strided over its queue)
 
 static_assert(5 * (kChunkBytes + sizeof(Shared) + kQueueBytes + 1024) <= 228 * 1024,
               "five bf16 sampler stream CTAs fit an SM's shared memory");
@@ -151,7 +149,7 @@ static_assert(Rec<Elt<uint16_t>>::BYTES % 16 == 0 && Rec<Elt<float>>::BYTES % 16
 
 // ------------------------------------------------- sampler records -----
 // Sampler only: one warp per packed row writes its row record (row_record)
-// before the stream kernel needs it; the exact kernel's queue starts empty.
+// before the stream kernel needs it.
 // (The other modes' stream CTAs compute their own record while their copy
 // is in flight: there it costs less than this launch and its wait, while
 // the sampler's record, with its parameter loads, costs its stream CTAs
@@ -160,8 +158,6 @@ template <typename TIn>
 __global__ void __launch_bounds__(256) sample_records_kernel(const VerifyParams p)
 {
     griddep_launch_dependents();
-    // the previous call's kernels have completed before this one starts
-    if (blockIdx.x == 0 && threadIdx.x == 0) p.ws_queue[0].x = 0;
     const int r = (blockIdx.x * 256 + threadIdx.x) >> 5;
     if (r >= p.R_cap) return;
     const RowInfo inf = row_record<TIn, MODE_SAMPLE>(p, r);
@@ -799,7 +795,6 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
     const int r = blockIdx.x;
     const int nchunk = p.nchunk;
 
-    griddep_launch_dependents();           // the exact kernel may wait for this one
     if (MODE != MODE_CONF && r >= p.R_cap) {
         // extra CTAs: the outputs of requests without a valid row range
         // (nothing of the stream kernel is read)
@@ -808,7 +803,6 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
     }
     griddep_wait();                        // the stream kernel's stores are visible
     if (tid == 0) {
-        sh.fin = 0;
         if (MODE != MODE_CONF) {
             sh.info = reinterpret_cast<const RowInfo *>(p.ws_info)[r];
             sh.info.valid = sh.info.valid && r < min(__ldg(p.cu_rows + p.B), p.R_cap);
@@ -843,12 +837,15 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
         cp.g = b.x; cp.w = b.y; cp.ncand = __float_as_int(b.z); cp.lev = b.w;
         parts[tid] = cp;
     }
-    if (MODE == MODE_SAMPLE && tid == 0 && !mbar_wait(&sh.mbar[0], 0)) {
-        // the records did not land in time: reported; one more bounded wait
-        // for the copies, and the row is not settled from them
-        set_status(p.status, SPEC_STATUS_TIMEOUT);
-        mbar_wait(&sh.mbar[0], 0);
-        sh.timeout = 1;
+    if (MODE == MODE_SAMPLE && tid == 0) {
+        if (!mbar_wait(&sh.mbar[0], 0)) {
+            // the records did not land in time: reported; one more bounded
+            // wait for the copies, and the row is not settled from them
+            set_status(p.status, SPEC_STATUS_TIMEOUT);
+            mbar_wait(&sh.mbar[0], 0);
+            sh.timeout = 1;
+        }
+        sh.ph[0] = 1u;      // the row streaming below continues from phase 1
     }
     csync();
     const RowInfo &info = sh.info;
@@ -984,20 +981,26 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
                                     reinterpret_cast<unsigned long long *>(cnt + kTally), gs, best, bi, sh);
             }
         }
-        if (whole && tid == 0) {
-            // the summaries cannot settle the row: queued for exact selects
-            // over the whole row (the exact kernel writes its token and runs
-            // its chain)
-            const int slot = atomicAdd(&p.ws_queue[0].x, 1);
-            p.ws_queue[1 + slot] = make_int4(r, __float_as_int(M), AMAX, 0);
-            sh.fin = 1;
+        if (whole) {
+            // The summaries cannot settle the row (a nucleus reaching below
+            // every chunk's counted values, a list overflow): exact selects
+            // over the whole row, streamed again through the scratch (its
+            // lists are spent).  After a timed-out records copy the
+            // barriers' state is not known: the row keeps its argmax
+            // (TIMEOUT is reported).
+            csync();
+            bi = INT_MAX;
+            if (!sh.timeout) {
+                const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row) & 15u);
+                const int h = min(mis ? static_cast<int>((16u - mis) / E::BYTES) : 0, p.V);
+                bi = exact_row_token<E>(row, p.V, h, M, info, nz, scratch, sh, sh.ph);
+            }
         }
         y = (bi == INT_MAX) ? AMAX : bi;
     }
 
     // ---------------------------------------------------- row results ---
     csync();
-    const bool queued = sh.fin != 0;
     if (tid == 0) {
         const float S = sh.S;
         if (p.row_max) p.row_max[r] = M;
@@ -1015,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
             }
             p.conf[r] = cf;
             p.draft_token[r] = s;
-        } else if (!queued) {
+        } else {
             // active vocabulary: the argmax column's full token id
             if (MODE == MODE_GREEDY && p.vocab_ids) y = __ldg(p.vocab_ids + AMAX);
             if (p.row_token) p.row_token[r] = y;
@@ -1023,7 +1026,7 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
             if (MODE == MODE_RELAXED || (MODE == MODE_GREEDY && p.margin)) p.ws_flag[r] = flag;
         }
     }
-    if (MODE != MODE_CONF && !queued && warp == 0) {
+    if (MODE != MODE_CONF && warp == 0) {
         // the request ticket: the row finishing its request runs the chain
         uint32_t t = 0;
         if (lane == 0) {
@@ -1034,62 +1037,6 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
         t = __shfl_sync(0xFFFFFFFFu, t, 0);
         if (t == static_cast<uint32_t>(info.k_b))
             chain_request<MODE>(p, info.b, info.k_b, r - info.pos, static_cast<uint32_t>(info.bad));
-    }
-}
-
-// ------------------------------------------------------- exact kernel ---
-
-// Rows the finish queued (a nucleus reaching below every chunk's counted
-// values, a candidate overflow): exact selects over the whole row, streamed
-// through shared memory by TMA, then the row's token and its request chain.
-// The CTAs stride over the queue; with an empty queue they leave at once.
-template <typename TIn>
-__global__ void __launch_bounds__(kThreads) exact_rows_kernel(const VerifyParams p)
-{
-    using E = Elt<TIn>;
-    extern __shared__ __align__(128) uint8_t smem[];
-    Shared &sh = *reinterpret_cast<Shared *>(smem);
-    uint8_t *stage = smem + sizeof(Shared);           // [2 * kRowStage]
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    griddep_wait();                                   // the finish kernel's queue
-    const int n = __ldcg(&p.ws_queue[0].x);
-    if (static_cast<int>(blockIdx.x) >= n) return;
-    if (tid == 0) {
-        sh.ph[0] = sh.ph[1] = 0u;
-        sh.timeout = 0;
-        mbar_init(&sh.mbar[0], 1);
-        mbar_init(&sh.mbar[1], 1);
-        fence_mbar_init();
-    }
-    for (int i = blockIdx.x; i < n; i += gridDim.x) {
-        const int4 q = __ldcg(p.ws_queue + 1 + i);
-        const int r = q.x;
-        if (tid == 0) sh.info = reinterpret_cast<const RowInfo *>(p.ws_info)[r];
-        csync();
-        const RowInfo &info = sh.info;
-        const float M = __int_as_float(q.y);
-        const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
-        const uint32_t mis = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(row) & 15u);
-        const int h = min(mis ? static_cast<int>((16u - mis) / E::BYTES) : 0, p.V);
-        const Noise nz{static_cast<uint32_t>(info.pos), info.rid, p.step, info.seed_lo, info.seed_hi};
-        const int32_t bi = exact_row_token<E>(row, p.V, h, M, info, nz, stage, sh, sh.ph);
-        const int32_t y = (bi == INT_MAX) ? q.z : bi;
-        if (tid == 0) {
-            if (p.row_token) p.row_token[r] = y;
-            p.ws_tok[r] = y;
-        }
-        if (warp == 0) {
-            uint32_t t = 0;
-            if (lane == 0) {
-                fence_acq_rel_gpu();
-                t = atomicAdd(p.ws_ticket + info.b, 1u);
-                if (t == static_cast<uint32_t>(info.k_b)) fence_acq_rel_gpu();
-            }
-            t = __shfl_sync(0xFFFFFFFFu, t, 0);
-            if (t == static_cast<uint32_t>(info.k_b))
-                chain_request<MODE_SAMPLE>(p, info.b, info.k_b, r - info.pos, static_cast<uint32_t>(info.bad));
-        }
-        csync();
     }
 }
 
@@ -1108,12 +1055,14 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
 {
     const size_t smem = kChunkBytes + sizeof(Shared) + ((MODE == MODE_SAMPLE && sizeof(TIn) == 2) ? kQueueBytes : 0);
     // the sampler's finish stages the records of the row's nchunk chunks
-    // after its scratch
-    const size_t smem_fin_max = sizeof(Shared) + kMaxChunks * sizeof(ChunkPart) + kFinScratch +
-                                (MODE == MODE_SAMPLE ? static_cast<size_t>(kMaxChunks) * Rec<Elt<TIn>>::BYTES : 0);
-    const size_t smem_fin = sizeof(Shared) + kMaxChunks * sizeof(ChunkPart) + kFinScratch +
-                            (MODE == MODE_SAMPLE ? static_cast<size_t>(p.nchunk) * Rec<Elt<TIn>>::BYTES : 0);
-    const size_t smem_exact = sizeof(Shared) + 2 * kRowStage;
+    // after its scratch; the scratch (and the records) also serve as the
+    // two stages of a row streamed again for exact selects
+    const size_t fin_base = sizeof(Shared) + kMaxChunks * sizeof(ChunkPart);
+    const size_t fin_stage = (MODE == MODE_SAMPLE) ? fin_base + 2 * kRowStage : 0;
+    const size_t smem_fin_max = std::max(fin_stage, fin_base + kFinScratch +
+        (MODE == MODE_SAMPLE ? static_cast<size_t>(kMaxChunks) * Rec<Elt<TIn>>::BYTES : 0));
+    const size_t smem_fin = std::max(fin_stage, fin_base + kFinScratch +
+        (MODE == MODE_SAMPLE ? static_cast<size_t>(p.nchunk) * Rec<Elt<TIn>>::BYTES : 0));
     auto kstream = stream_chunks_kernel<TIn, MODE>;
     auto kfin = finish_rows_kernel<TIn, MODE>;
     // raise the dynamic shared-memory limits and prefer shared memory over
@@ -1134,11 +1083,6 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
         e = cudaFuncSetAttribute(kfin, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem_fin_max));
         if (e != cudaSuccess) return e;
-        if (MODE == MODE_SAMPLE) {
-            e = cudaFuncSetAttribute(exact_rows_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem_exact));
-            if (e != cudaSuccess) return e;
-        }
         done[dev] = true;
     }
     const int rows = (MODE == MODE_CONF) ? p.n_rows : p.R_cap;
@@ -1179,17 +1123,7 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     cf.stream = stream;
     cf.attrs = attr;
     cf.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cf, kfin, p);
-    if (e != cudaSuccess || MODE != MODE_SAMPLE) return e;
-    // rows for exact selects: usually none, the CTAs then leave at once
-    cudaLaunchConfig_t cx = {};
-    cx.gridDim = dim3(static_cast<unsigned>(std::min(rows, kExactCtas)), 1, 1);
-    cx.blockDim = dim3(kThreads, 1, 1);
-    cx.dynamicSmemBytes = smem_exact;
-    cx.stream = stream;
-    cx.attrs = attr;
-    cx.numAttrs = 1;
-    return cudaLaunchKernelEx(&cx, exact_rows_kernel<TIn>, p);
+    return cudaLaunchKernelEx(&cf, kfin, p);
 }
 
 // Rows at or above which bf16 relaxed top-K verification takes the row

@@ -50,8 +50,7 @@ def test_workspace_bytes(sv):
     # 640 rows of V = 152064 bf16: 10 chunks of 32 KiB per row
     base = 3 * 2560 + 512 + 640 * 64 + 640 * 10 * 32
     assert L.spec_workspace_bytes(640, 128, 152064, 1, 0) == base
-    queue = ((641 * 16 + 255) // 256) * 256                 # rows queued for exact selects
-    assert L.spec_workspace_bytes(640, 128, 152064, 1, 1) == base + 640 * 10 * 512 * 8 + queue
+    assert L.spec_workspace_bytes(640, 128, 152064, 1, 1) == base + 640 * 10 * 512 * 8
     assert L.spec_workspace_bytes(640, 128, 152064, 0, 0) == 3 * 2560 + 512 + 640 * 64 + 640 * 19 * 32
     assert L.spec_workspace_bytes(0, 128, 100, 1, 0) == 0
     assert L.spec_workspace_bytes(10, 0, 100, 1, 1) == 0

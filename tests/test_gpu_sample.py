@@ -201,8 +201,8 @@ def test_pure_top_p_rows_not_vector_aligned(dtype):
 
 def test_many_diffuse_rows():
     """Every row's nucleus is diffuse (80 requests): most rows are settled
-    from the counted values, and any the finish queues are taken by the
-    exact kernel's CTAs striding over the queue."""
+    from the counted values, and any they cannot settle take exact selects
+    over the whole row in the same finish CTA."""
     sv = need_gpu()
     vb = W.ragged_batch(seed=47, B=80, k_max=4, V=152064, dtype="bf16")
     check(sv, vb, params(vb.B, 1.0, 0, 0.9, 0.0, seed=9))
