@@ -27,17 +27,17 @@ size_t elt_bytes(int dtype) { return dtype == SPEC_BF16 ? 2 : 4; }
 
 struct WsLayout {
     int32_t *tok, *flag;
-    uint32_t *ticket, *rticket;
+    uint32_t *ticket;
     void *info, *part, *cand;
 };
 
-// tok [R_cap] | flag [R_cap] | ticket [B] | rticket [R_cap] | info [R_cap * 64 B] |
+// tok [R_cap] | flag [R_cap] | ticket [B] | info [R_cap * 64 B] |
 // part [R_cap * nchunk * 32 B] | cand (sampler only); 256-byte aligned
 size_t ws_bytes(int32_t R_cap, int32_t B, int32_t V, int elt, bool sampling)
 {
     const size_t R = static_cast<size_t>(R_cap);
     const size_t rc = R * static_cast<size_t>(chunks_per_row(V, elt));
-    size_t n = 3 * align256(R * 4) + align256(static_cast<size_t>(B) * 4) + align256(R * 64) +
+    size_t n = 2 * align256(R * 4) + align256(static_cast<size_t>(B) * 4) + align256(R * 64) +
                align256(rc * 32);
     if (sampling) n += align256(rc * kWsCandCap * 8);
     return n;
@@ -55,8 +55,6 @@ WsLayout ws_layout(void *ws, int32_t R_cap, int32_t B, int32_t V, int elt, bool 
     p += align256(R * 4);
     l.ticket = reinterpret_cast<uint32_t *>(p);
     p += align256(static_cast<size_t>(B) * 4);
-    l.rticket = reinterpret_cast<uint32_t *>(p);
-    p += align256(R * 4);
     l.info = p;
     p += align256(R * 64);
     l.part = p;
@@ -114,7 +112,6 @@ VerifyParams base_params(const spec_batch *b, const spec_outputs *o, void *ws, b
     p.ws_tok = l.tok;
     p.ws_flag = l.flag;
     p.ws_ticket = l.ticket;
-    p.ws_rticket = l.rticket;
     p.ws_info = l.info;
     p.ws_part = l.part;
     p.ws_cand = l.cand;
@@ -306,7 +303,6 @@ int spec_draft_confidence(const spec_draft *d, const spec_allocation *o, void *w
     p.ws_tok = l.tok;
     p.ws_flag = l.flag;
     p.ws_ticket = l.ticket;
-    p.ws_rticket = l.rticket;
     p.ws_info = l.info;
     p.ws_part = l.part;
     p.nchunk = chunks_per_row(d->V, elt);

@@ -64,7 +64,6 @@ struct VerifyParams {
     int32_t *ws_tok;             // [R_cap] per-row target token
     int32_t *ws_flag;            // [R_cap] per-row relaxed acceptance
     uint32_t *ws_ticket;         // [B] arrivals per request (zero between calls)
-    uint32_t *ws_rticket;        // [R_cap] arrivals per row (zero between calls)
     void *ws_info;               // [R_cap] row records (64 bytes each)
     void *ws_part;               // [R_cap * nchunk] chunk partials (32 bytes each)
     void *ws_cand;               // [R_cap * nchunk * kWsCandCap] (value, index) pairs

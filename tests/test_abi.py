@@ -48,15 +48,15 @@ def test_package_exposes_a_binding_per_entry_point(sv):
 def test_workspace_bytes(sv):
     L = sv.load_library()
     # 640 rows of V = 152064 bf16: 10 chunks of 32 KiB per row
-    base = 3 * 2560 + 512 + 640 * 64 + 640 * 10 * 32
+    base = 2 * 2560 + 512 + 640 * 64 + 640 * 10 * 32
     assert L.spec_workspace_bytes(640, 128, 152064, 1, 0) == base
     assert L.spec_workspace_bytes(640, 128, 152064, 1, 1) == base + 640 * 10 * 512 * 8
-    assert L.spec_workspace_bytes(640, 128, 152064, 0, 0) == 3 * 2560 + 512 + 640 * 64 + 640 * 19 * 32
+    assert L.spec_workspace_bytes(640, 128, 152064, 0, 0) == 2 * 2560 + 512 + 640 * 64 + 640 * 19 * 32
     assert L.spec_workspace_bytes(0, 128, 100, 1, 0) == 0
     assert L.spec_workspace_bytes(10, 0, 100, 1, 1) == 0
     assert L.spec_workspace_bytes(10, 1, 100, 9, 1) == 0
     assert L.spec_draft_workspace_bytes(16, 7, 151552, 1) == (
-        3 * 512 + 256 + 112 * 64 + ((112 * 10 * 32 + 255) // 256) * 256)
+        2 * 512 + 256 + 112 * 64 + ((112 * 10 * 32 + 255) // 256) * 256)
 
 
 def test_host_argument_errors_launch_nothing(sv):
