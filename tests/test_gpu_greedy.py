@@ -95,7 +95,7 @@ def test_greedy_without_row_outputs_and_repeat_calls():
     assert int(ws.sum().item()) >= 0
     R = vb.logits.shape[0]
     off = 2 * ((R * 4 + 255) // 256 * 256)                 # tok, flag
-    tick = (vb.B * 4 + 255) // 256 * 256 + (R * 4 + 255) // 256 * 256   # request + row tickets
+    tick = (vb.B * 4 + 255) // 256 * 256                  # request tickets
     assert ws[off:off + tick].sum().item() == 0
 
 
