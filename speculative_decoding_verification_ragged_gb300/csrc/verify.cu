@@ -157,6 +157,12 @@ static_assert(Rec<Elt<uint16_t>>::BYTES % 16 == 0 && Rec<Elt<float>>::BYTES % 16
 template <typename TIn>
 __global__ void __launch_bounds__(256) sample_records_kernel(const VerifyParams p)
 {
+    // Launched as a programmatic dependent of whatever kernel precedes the
+    // call (the previous call's finish, say), so its CTAs are resident when
+    // that one ends.  Nothing is read before that kernel has completed, and
+    // the stream kernel is released only then: its chunk copies read the
+    // logits before it waits for this kernel.
+    griddep_wait();
     griddep_launch_dependents();
     const int r = (blockIdx.x * 256 + threadIdx.x) >> 5;
     if (r >= p.R_cap) return;
@@ -795,6 +801,9 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
     const int r = blockIdx.x;
     const int nchunk = p.nchunk;
 
+    // a following call's first kernel may become resident (it waits for
+    // this grid's completion before it reads anything)
+    griddep_launch_dependents();
     if (MODE != MODE_CONF && r >= p.R_cap) {
         // extra CTAs: the outputs of requests without a valid row range
         // (nothing of the stream kernel is read)
@@ -1089,15 +1098,19 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     // the finish kernel's extra CTAs write the outputs of requests without a
     // valid row range
     const int req_blocks = (MODE == MODE_CONF) ? 0 : (p.B + kThreads - 1) / kThreads;
-    if (MODE == MODE_SAMPLE) {
-        sample_records_kernel<TIn><<<static_cast<unsigned>((static_cast<int64_t>(rows) * 32 + 255) / 256), 256, 0,
-                                     stream>>>(p);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (MODE == MODE_SAMPLE) {
+        cudaLaunchConfig_t cr = {};
+        cr.gridDim = dim3(static_cast<unsigned>((static_cast<int64_t>(rows) * 32 + 255) / 256), 1, 1);
+        cr.blockDim = dim3(256, 1, 1);
+        cr.stream = stream;
+        cr.attrs = attr;
+        cr.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cr, sample_records_kernel<TIn>, p);
+        if (e != cudaSuccess) return e;
+    }
     // one CTA per (row, chunk); the entry points bound rows * nchunk by 2^31 - 1
     cudaLaunchConfig_t cfg = {};
     if (MODE == MODE_SAMPLE)
@@ -1110,9 +1123,9 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    // the first kernel of a call runs in plain stream order, after
-    // everything the caller queued before (the previous call included); the
-    // sampler's follows its records kernel
+    // the first kernel of a greedy-family call runs in plain stream order,
+    // after everything the caller queued before (the previous call
+    // included); the sampler's follows its records kernel
     cfg.numAttrs = (MODE == MODE_SAMPLE) ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kstream, p);
     if (e != cudaSuccess) return e;
