@@ -217,11 +217,15 @@ def _batch(logits, V, B, k_max, R_cap, cu_rows, draft_ids) -> Batch:
 
 
 def _outputs(B, k_max, R_cap, device, rows: bool, stats) -> tuple:
+    # the request outputs and the status word in one int32 buffer
+    # ("request_block"), so one copy brings them to the host
+    blk = torch.zeros(B * (k_max + 3) + 1, dtype=torch.int32, device=device)
     res = {
-        "accepted_len": torch.empty(B, dtype=torch.int32, device=device),
-        "out_tokens": torch.empty(B, k_max + 1, dtype=torch.int32, device=device),
-        "next_token": torch.empty(B, dtype=torch.int32, device=device),
-        "status": torch.zeros(1, dtype=torch.int32, device=device),
+        "accepted_len": blk[:B],
+        "out_tokens": blk[B:B * (k_max + 2)].view(B, k_max + 1),
+        "next_token": blk[B * (k_max + 2):B * (k_max + 3)],
+        "status": blk[B * (k_max + 3):],
+        "request_block": blk,
     }
     if rows:
         res["row_max"] = torch.empty(R_cap, dtype=torch.float32, device=device)
