@@ -217,3 +217,30 @@ def test_unfiltered_rows_not_block_aligned(dtype):
     vb = W.ragged_batch(seed=41, B=5, k_max=3, V=V, dtype=dtype, ld=V + 3)
     for T in (0.5, 1.0):
         check(sv, vb, params(vb.B, T, 0, 1.0, 0.0, seed=3))
+
+
+def test_back_to_back_calls_share_a_workspace():
+    """Three different batches of one shape queued back to back on one stream
+    with one workspace and no synchronisation between them: the records
+    kernel of a call waits for the previous call's finish before it
+    rewrites the row records, so every call matches the oracle on its own
+    inputs."""
+    sv = need_gpu()
+    cases = []
+    for i, (T, k, tp, mp) in enumerate([(1.0, 50, 1.0, 0.0), (0.5, 0, 0.9, 0.0), (0.0, 0, 1.0, 0.0)]):
+        vb = W.ragged_batch(seed=60 + i, B=24, k_max=4, V=152064, dtype="bf16",
+                            k_values=np.array([4, 0, 3, 1, 2, 4] * 4))
+        cases.append((vb, params(vb.B, T, k, tp, mp, seed=70 + i, step=i)))
+    R = max(vb.logits.shape[0] for vb, _ in cases)
+    B = max(vb.B for vb, _ in cases)
+    ws = sv.new_workspace(R, B, 152064, "bf16", sampling=True)
+    outs = []
+    for vb, p in cases:
+        assert vb.logits.shape[0] == R and vb.B == B
+        outs.append(run_sample(sv, vb, p, rows=True, workspace=ws))
+    for (vb, p), res in zip(cases, outs):
+        ref = oracle.verify_sample(vb.logits, vb.dtype, vb.V, vb.B, vb.k_max, vb.cu_rows,
+                                   vb.draft_ids, p)
+        got = host(res)
+        assert compare_sampled(vb, p, got, ref, label="back to back") == 0
+        assert got["status"][0] == ref.status
