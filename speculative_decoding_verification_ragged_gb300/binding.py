@@ -251,7 +251,10 @@ def verify_greedy(logits, cu_rows, draft_ids, *, V: int, B: int, k_max: int,
                   R_cap: Optional[int] = None, workspace=None, rows: bool = True, stats=None,
                   stream=None) -> dict:
     """spec_verify_greedy: fused max/LSE/argmax per row, then greedy prefix
-    acceptance per request.  Returns a dict of device tensors."""
+    acceptance per request.  Returns a dict of device tensors: accepted_len,
+    out_tokens, next_token and status are views of one int32 block
+    ("request_block", in that order), so one copy brings them to the host;
+    with rows=True also row_max, row_lse, row_argmax and row_token."""
     L = load_library()
     R_cap = R_cap or B * (k_max + 1)
     ws = workspace if workspace is not None else new_workspace(
