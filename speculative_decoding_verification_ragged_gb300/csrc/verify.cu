@@ -419,13 +419,14 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
     griddep_launch_dependents();
     // The sampler takes chunk-major order: a chunk's cost depends on its
     // row's filters, and this spreads every row's chunks evenly over the
-    // grid, with the short tail chunks in the last wave.  Uniform modes keep
-    // row-major order.  The grid is two-dimensional with the faster index in
-    // x (sampler: x = row, y = chunk; else x = chunk, y = row), so the order
-    // comes without divisions; row-major grids of more than 65535 rows are
-    // one-dimensional.
+    // grid, with the short tail chunks in the last wave.  So does the
+    // confidence, whose grid is little more than one wave: its last CTAs are
+    // then short tail chunks.  The other modes keep row-major order.  The
+    // grid is two-dimensional with the faster index in x (chunk-major: x =
+    // row, y = chunk; else x = chunk, y = row), so the order comes without
+    // divisions; row-major grids of more than 65535 rows are one-dimensional.
     int r, c;
-    if (MODE == MODE_SAMPLE) {
+    if (MODE == MODE_SAMPLE || MODE == MODE_CONF) {
         r = static_cast<int>(blockIdx.x);
         c = static_cast<int>(blockIdx.y);
     } else if (gridDim.y > 1 || gridDim.x == static_cast<unsigned>(nchunk)) {
@@ -1113,7 +1114,7 @@ static cudaError_t launch_t(const VerifyParams &p, cudaStream_t stream)
     }
     // one CTA per (row, chunk); the entry points bound rows * nchunk by 2^31 - 1
     cudaLaunchConfig_t cfg = {};
-    if (MODE == MODE_SAMPLE)
+    if (MODE == MODE_SAMPLE || MODE == MODE_CONF)
         cfg.gridDim = dim3(static_cast<unsigned>(rows), static_cast<unsigned>(p.nchunk), 1);
     else if (rows <= 65535)
         cfg.gridDim = dim3(static_cast<unsigned>(p.nchunk), static_cast<unsigned>(rows), 1);
