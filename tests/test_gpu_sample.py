@@ -244,3 +244,14 @@ def test_back_to_back_calls_share_a_workspace():
         got = host(res)
         assert compare_sampled(vb, p, got, ref, label="back to back") == 0
         assert got["status"][0] == ref.status
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 1_048_000), ("f32", 524_000)])
+def test_longest_rows(dtype, V):
+    """Rows near the 2 MiB limit (64 chunks): bf16 top-p-alone rows span more
+    chunks than the finish stages counts for and take the exact whole-row
+    selects; the other filters settle from the chunk summaries as usual."""
+    sv = need_gpu()
+    vb = W.ragged_batch(seed=V % 1000, B=2, k_max=2, V=V, dtype=dtype, k_values=np.array([2, 1]))
+    for T, k, tp, mp in [(1.0, 0, 0.9, 0.0), (0.7, 50, 1.0, 0.05), (0.7, 0, 1.0, 0.0), (0.0, 0, 1.0, 0.0)]:
+        check(sv, vb, params(vb.B, T, k, tp, mp, seed=int(T * 10) + k), label="V=%d %s" % (V, dtype))
