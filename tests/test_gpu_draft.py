@@ -147,3 +147,18 @@ def test_adaptive_verify_pipeline_on_device():
     np.testing.assert_array_equal(got["accepted_len"], ref.accepted_len)
     np.testing.assert_array_equal(got["next_token"], ref.next_token)
     assert (got["accepted_len"] <= a["k_alloc"]).all()
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 1_048_000), ("f32", 524_000), ("bf16", 1000)])
+def test_confidence_row_lengths(dtype, V):
+    """Draft rows near the 2 MiB limit (64 chunks) and far below one chunk:
+    the confidence's chunk-major grid and its combine over every chunk."""
+    sv = need_gpu()
+    db = W.mtp_adaptive(seed=V % 997, B=3, k=4, V=V, planted_draft=True, dtype=dtype)
+    ref = oracle.draft_confidence(db.draft_logits, dtype, db.V, db.B, db.k, threshold=0.3)
+    got = run_conf(sv, db)
+    np.testing.assert_allclose(got["conf"], ref.conf, rtol=CONF_RTOL, atol=0)
+    vals = W.bf16_bits_to_f32(db.draft_logits) if dtype == "bf16" else db.draft_logits
+    np.testing.assert_array_equal(got["draft_token"], np.argmax(vals[:, :db.V], axis=1))
+    check_alloc(got, ref, db.B, db.k, 0.3, 0)
+    assert got["status"][0] == 0
