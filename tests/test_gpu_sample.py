@@ -255,3 +255,17 @@ def test_longest_rows(dtype, V):
     vb = W.ragged_batch(seed=V % 1000, B=2, k_max=2, V=V, dtype=dtype, k_values=np.array([2, 1]))
     for T, k, tp, mp in [(1.0, 0, 0.9, 0.0), (0.7, 50, 1.0, 0.05), (0.7, 0, 1.0, 0.0), (0.0, 0, 1.0, 0.0)]:
         check(sv, vb, params(vb.B, T, k, tp, mp, seed=int(T * 10) + k), label="V=%d %s" % (V, dtype))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_more_rows_than_a_grid_dimension_holds(dtype):
+    """More than 65535 packed rows of a short vocabulary, mixed filters: the
+    records kernel's and the chunk-major stream grid's row index past 2^16,
+    and 14000 request tickets."""
+    sv = need_gpu()
+    vb = W.ragged_batch(seed=71, B=14000, k_max=8, V=64, dtype=dtype)
+    assert vb.R > 65535
+    rng = np.random.default_rng(72)
+    p = W.random_sample_params(rng, vb.B, top_ks=(0, 5, 20), top_ps=(1.0, 0.9), min_ps=(0.0, 0.05))
+    got, _ = check(sv, vb, p, label="R=%d %s" % (vb.R, dtype))
+    assert got["n_differ"] == 0
