@@ -112,6 +112,23 @@ def test_relaxed_topk_ragged(dtype):
     assert got["status"][0] == ref.status == 0x40
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_relaxed_more_rows_than_a_grid_dimension_holds(dtype):
+    """More than 65535 packed rows of a short vocabulary: bf16 takes the row
+    path (one CTA per row, a one-dimensional grid), fp32 the chunk path's
+    one-dimensional row-major grid."""
+    sv = need_gpu()
+    vb = W.ragged_batch(seed=73, B=14000, k_max=8, V=64, dtype=dtype, p_top=0.4)
+    assert vb.R > 65535
+    K = np.random.default_rng(74).integers(1, 6, size=vb.B).astype(np.int32)
+    ref = oracle.verify_relaxed(vb.logits, vb.dtype, vb.V, vb.B, vb.k_max, vb.cu_rows,
+                                vb.draft_ids, K)
+    got = host(run_relaxed(sv, vb, K))
+    assert_requests_equal(got, ref)
+    np.testing.assert_array_equal(got["row_argmax"][:vb.R], ref.rows["row_argmax"])
+    assert got["status"][0] == ref.status
+
+
 def test_relaxed_eagle_workload_with_fused_stats():
     """EAGLE-relaxed: B=256, k=5, V=152064 bf16, planted peaks, K=4; counters
     accumulated over 20 seeded steps by the fused path and by
