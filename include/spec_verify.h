@@ -55,6 +55,15 @@
  *     (ignored on bonus rows); ids outside [0, V) are mismatches, not errors.
  *   - Argmax ties resolve to the lowest index; -0.0 equals +0.0.
  *   - Calls that share a workspace must be ordered on one stream.
+ *   - Launch order: each call's kernels follow one another by programmatic
+ *     dependent launch.  spec_verify_sample's first kernel is itself a
+ *     programmatic dependent of whatever kernel precedes it on the stream:
+ *     its blocks may become resident early, but they read nothing and
+ *     release nothing before that kernel has completed, so inputs written by
+ *     it are seen.  A call's last kernel lets the next kernel on the stream
+ *     launch early in the same way; a kernel that reads this call's outputs
+ *     must wait (griddepcontrol.wait) if it is itself launched as a
+ *     programmatic dependent.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
