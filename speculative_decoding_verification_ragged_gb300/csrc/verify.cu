@@ -258,13 +258,13 @@ __device__ void summary_top_p_bf16(const VerifyParams &p, const uint4 *body, con
         if (xv >= zbot) list(xv, ix, nz.score(xv, ix, f.invT));
     }
     if ((g.a0 & 3) == 0) {
-        // The body covers whole Philox blocks.  Pass A counts the values and
-        // queues, per warp, the blocks that may list an element: one in the
-        // counted range, and a block maximum that reaches s_top with the
-        // largest noise.  About a third of the blocks qualify, but some lane
-        // of a warp nearly always needs its block, so a lane-by-lane skip
-        // would draw every block; pass B draws only the queued ones, packed
-        // by ballots.
+        // The body covers whole Philox blocks.  Pass A queues, per warp, the
+        // blocks with an element in the counted range (about half of them):
+        // some lane of a warp nearly always has one, so a lane-by-lane pass
+        // would visit every block.  Pass B takes only the queued blocks,
+        // packed by ballots: it counts their elements in the range and, if
+        // the block's maximum can reach s_top with the largest noise, draws
+        // its noise and lists the elements that reach it.
         const int lane = tid & 31;
         const unsigned lt = (1u << lane) - 1u;
         uint16_t *wq = reinterpret_cast<uint16_t *>(&sh + 1) + (tid >> 5) * kQueuePerWarp;
@@ -273,14 +273,10 @@ __device__ void summary_top_p_bf16(const VerifyParams &p, const uint4 *body, con
             const int i = i0 + lane;
             bool q0 = false, q1 = false;
             if (i < g.nb) {
-                float x[8];
-                E::unpack(body[i], x);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) count(x[q]);
-                const float b0 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-                const float b1 = fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]));
-                q0 = b0 >= zbot && !(fmaf(b0, f.invT, kGumbelMax) < s_top);
-                q1 = b1 >= zbot && !(fmaf(b1, f.invT, kGumbelMax) < s_top);
+                const uint4 v = body[i];
+                const uint32_t w0 = max_bf16x2(v.x, v.y), w1 = max_bf16x2(v.z, v.w);
+                q0 = fmaxf(bf_lo(w0), bf_hi(w0)) >= zbot;
+                q1 = fmaxf(bf_lo(w1), bf_hi(w1)) >= zbot;
             }
             const unsigned m0 = __ballot_sync(0xFFFFFFFFu, q0), m1 = __ballot_sync(0xFFFFFFFFu, q1);
             if (q0) wq[nq + __popc(m0 & lt)] = static_cast<uint16_t>(2 * i);
@@ -295,7 +291,11 @@ __device__ void summary_top_p_bf16(const VerifyParams &p, const uint4 *body, con
             const uint32_t blk = wq[e];
             const uint2 u = halves[blk];
             const float x[4] = {bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y)};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) count(x[j]);
             const float bm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            // no element of the block can reach s_top (the noise is bounded)
+            if (fmaf(bm, f.invT, kGumbelMax) < s_top) continue;
             const float D = ex2((bm * f.invT - s_top) * kLog2e);
             const float t = fmaf(-D, 16777216.f, 16777215.f) * 0.5f;
             const uint32_t kthr = (t >= 2.f) ? static_cast<uint32_t>(t) - 1u : 0u;
