@@ -522,10 +522,10 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
     chunk_reduce<MODE>(tmax, targ, tsum, tcnt, need_sum, sh);
 
     const int64_t rc = static_cast<int64_t>(r) * nchunk + c;
-    if (MODE == MODE_SAMPLE && info.T > 0.f) {
+    // (the summary's fields of sh.part are written by thread 0, the thread
+    // that stores the part: no barrier before the store)
+    if (MODE == MODE_SAMPLE && info.T > 0.f)
         summary_sampler<E>(p, info, body, g, thread_max, thread_arg, tsec, rc, sh);
-        csync();
-    }
     if (tid == 0) reinterpret_cast<ChunkPart *>(p.ws_part)[rc] = sh.part;
 }
 
