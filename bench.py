@@ -148,8 +148,28 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm -----
 
+# Row classes for profiling the sampler one filter kind at a time (every
+# request given the same filters); "mix" is the benchmark's workload.
+ROW_CLASSES = {
+    "mix": {},
+    "greedy": dict(temperatures=(0.0,)),
+    "topk": dict(temperatures=(1.0,), top_ks=(50,), top_ps=(1.0,), min_ps=(0.0,)),
+    "minp": dict(temperatures=(1.0,), top_ks=(0,), top_ps=(1.0,), min_ps=(0.05,)),
+    "topp1": dict(temperatures=(1.0,), top_ks=(0,), top_ps=(0.9,), min_ps=(0.0,)),
+    "topp05": dict(temperatures=(0.5,), top_ks=(0,), top_ps=(0.9,), min_ps=(0.0,)),
+    "unfiltered": dict(temperatures=(1.0,), top_ks=(0,), top_ps=(1.0,), min_ps=(0.0,)),
+}
+ROW_CLASS = "mix"
+
+
+def workload_name() -> str:
+    if ROW_CLASS == "mix":
+        return WORKLOAD
+    return WORKLOAD + " -- profiling variant: every request " + ROW_CLASS
+
+
 def make_inputs(seed: int):
-    vb, p = W.stochastic(seed=seed)
+    vb, p = W.stochastic(seed=seed, **ROW_CLASSES[ROW_CLASS])
     return vb, p
 
 
@@ -336,7 +356,7 @@ def run_ours(args) -> None:
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": B * world, "rows_per_step": R,
+            "config": {"workload": workload_name(), "global_batch": B * world, "rows_per_step": R,
                        "vocab": V, "draft_tokens": K, "parallelism": "replicas" if world > 1 else "1 gpu",
                        "l2": "inputs rotate over %d device copies of %.1f MB each (> 129 MB L2)"
                              % (nsets, R * V * 2 / 1e6)},
@@ -748,7 +768,7 @@ def run_reference(args) -> None:
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "global_batch": B,
+        "data": "synthetic", "config": {"workload": workload_name(), "global_batch": B,
                                         "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 3), "unit": "rows/s", "cores": cores,
                          "kind": "oracle",
@@ -769,9 +789,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-entries", action="store_true", help="skip the other entry points")
     ap.add_argument("--entry-launches", type=int, default=50)
+    ap.add_argument("--row-class", choices=sorted(ROW_CLASSES), default="mix",
+                    help="every request's filters alike, for profiling (default: the benchmark's mix)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    global ROW_CLASS
+    ROW_CLASS = args.row_class
     if args.impl == "reference":
         run_reference(args)
     else:
