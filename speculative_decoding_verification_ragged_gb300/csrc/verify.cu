@@ -344,9 +344,30 @@ __device__ void summary_sampler(const VerifyParams &p, const RowInfo &info, cons
 {
     constexpr int VEC = E::VEC;
     const int tid = threadIdx.x;
+    const float m_c = sh.part.m;
+    // top-k / min-p (and fp32 top-p alone), the commonest filtered rows,
+    // first: they need neither 1/T nor the row's noise key
+    const bool use_k = info.top_k > 0 && info.top_k < p.V, use_m = info.min_p > 0.f;
+    if (use_k || use_m || (E::BYTES == 4 && info.top_p < 1.f)) {
+        // per thread slot (the thread's elements of the chunk, extras
+        // included) its maximum, its second largest element and the
+        // maximum's offset in the chunk; for fp32 top-p alone also the
+        // chunk's mass at temperature T
+        Rec<E>::put(reinterpret_cast<uint8_t *>(reinterpret_cast<Cand *>(p.ws_cand) + rc * kCandCap), tid,
+                    thread_max, thread_sec,
+                    static_cast<uint16_t>(thread_max > -INFINITY ? thread_arg - g.e0 : 0));
+        if (!use_k && !use_m && m_c > -INFINITY) {
+            const Filter f(info, p.V);
+            const float T = f.T;
+            float mass = (T != 1.0f) ? chunk_mass<E>(body, g.nb, m_c, f.sc) : 0.f;
+            if (T != 1.0f && tid < g.n_extra) mass += ex2((sh.extras_v[tid] - m_c) * f.sc);
+            if (T != 1.0f) mass = block_sum(mass, sh);
+            if (tid == 0) sh.part.w = (T != 1.0f) ? mass : sh.part.s;
+        }
+        return;
+    }
     const Filter f(info, p.V);
     const float T = f.T, invT = f.invT;
-    const float m_c = sh.part.m;
     const Noise nz{static_cast<uint32_t>(info.pos), info.rid, p.step, info.seed_lo, info.seed_hi};
     if (f.unfiltered) {
         if (!(m_c > -INFINITY)) return;        // only -inf here: nothing to draw from
@@ -378,24 +399,9 @@ __device__ void summary_sampler(const VerifyParams &p, const RowInfo &info, cons
         if (tid == 0) { sh.part.g = best; sh.part.aux = bi; }
         return;
     }
-    if constexpr (E::BYTES == 2) {
-        if (f.pure_p) {
-            if (m_c > -INFINITY) summary_top_p_bf16<E>(p, body, g, f, nz, rc, sh);
-            return;
-        }
-    }
-    // top-k / min-p, fp32 top-p alone: per thread slot (the thread's elements
-    // of the chunk, extras included) its maximum, its second largest element
-    // and the maximum's offset in the chunk; for fp32 top-p alone also the
-    // chunk's mass at temperature T
-    Rec<E>::put(reinterpret_cast<uint8_t *>(reinterpret_cast<Cand *>(p.ws_cand) + rc * kCandCap), tid,
-                thread_max, thread_sec, static_cast<uint16_t>(thread_max > -INFINITY ? thread_arg - g.e0 : 0));
-    if (f.pure_p && m_c > -INFINITY) {
-        float mass = (T != 1.0f) ? chunk_mass<E>(body, g.nb, m_c, f.sc) : 0.f;
-        if (T != 1.0f && tid < g.n_extra) mass += ex2((sh.extras_v[tid] - m_c) * f.sc);
-        if (T != 1.0f) mass = block_sum(mass, sh);
-        if (tid == 0) sh.part.w = (T != 1.0f) ? mass : sh.part.s;
-    }
+    // bf16 top-p alone (the only case left)
+    if constexpr (E::BYTES == 2)
+        if (m_c > -INFINITY) summary_top_p_bf16<E>(p, body, g, f, nz, rc, sh);
 }
 
 // ------------------------------------------------------ stream kernel ----
