@@ -149,10 +149,14 @@ def test_adaptive_verify_pipeline_on_device():
     assert (got["accepted_len"] <= a["k_alloc"]).all()
 
 
-@pytest.mark.parametrize("dtype,V", [("bf16", 1_048_000), ("f32", 524_000), ("bf16", 1000)])
+@pytest.mark.parametrize("dtype,V", [("bf16", 1_048_000), ("f32", 524_000), ("bf16", 1000),
+                                     ("bf16", 16_385), ("bf16", 262_144), ("bf16", 262_145),
+                                     ("f32", 131_072), ("f32", 131_073)])
 def test_confidence_row_lengths(dtype, V):
-    """Draft rows near the 2 MiB limit (64 chunks) and far below one chunk:
-    the confidence's chunk-major grid and its combine over every chunk."""
+    """Draft rows near the 2 MiB limit (64 chunks), far below one chunk, of
+    exactly 16 chunks and one element more (a last chunk of one element, as
+    in the 16 385-element bf16 row); the chunk-major grid and the combine
+    over every chunk."""
     sv = need_gpu()
     db = W.mtp_adaptive(seed=V % 997, B=3, k=4, V=V, planted_draft=True, dtype=dtype)
     ref = oracle.draft_confidence(db.draft_logits, dtype, db.V, db.B, db.k, threshold=0.3)
@@ -162,3 +166,29 @@ def test_confidence_row_lengths(dtype, V):
     np.testing.assert_array_equal(got["draft_token"], np.argmax(vals[:, :db.V], axis=1))
     check_alloc(got, ref, db.B, db.k, 0.3, 0)
     assert got["status"][0] == 0
+
+
+@pytest.mark.parametrize("dtype,V,off", [("bf16", 151_552, 3), ("bf16", 20_000, 1), ("f32", 70_001, 2)])
+def test_confidence_unaligned_rows(dtype, V, off):
+    """Rows that start off a 16-byte boundary (a view into wider rows): every
+    chunk's head and tail elements come from plain loads, and the selected
+    tokens' logits from the unaligned rows."""
+    sv = need_gpu()
+    db = W.mtp_adaptive(seed=V % 991, B=4, k=3, V=V, planted_draft=True, dtype=dtype)
+    x = logits_tensor(db.draft_logits, dtype)
+    # rows of V + 8 elements whose first starts `off` elements into the
+    # allocation (one spare row keeps the last one inside it)
+    Q, ld = x.shape[0], V + 8
+    wide = torch.zeros(((Q + 1) * ld,), dtype=x.dtype, device=x.device)
+    view = torch.as_strided(wide, (Q, ld), (ld, 1), off)
+    view[:, :V] = x[:, :V]
+    sel = np.random.default_rng(V).integers(0, V, size=db.B * db.k).astype(np.int32)
+    for selected in (None, sel):
+        ref = oracle.draft_confidence(db.draft_logits, dtype, db.V, db.B, db.k, selected=selected,
+                                      threshold=0.3)
+        got = host(sv.draft_confidence(view, V=V, B=db.B, k=db.k,
+                                       selected=None if selected is None else t(selected),
+                                       threshold=0.3))
+        np.testing.assert_allclose(got["conf"], ref.conf, rtol=CONF_RTOL, atol=1e-30)
+        check_alloc(got, ref, db.B, db.k, 0.3, 0)
+        assert got["status"][0] == 0
