@@ -385,16 +385,30 @@ __device__ __forceinline__ void keep_best(float s, int32_t ix, float &best, int3
     if (s > best || (s == best && ix < bi)) { best = s; bi = ix; }
 }
 
-// Scores of the VEC elements of one vector starting at element `base`, a
-// multiple of 4 (the vector covers whole Philox blocks), whose largest value
-// is vm.  An element can only reach `best` if its Gumbel noise -log(-log u)
-// reaches best - z/T, i.e. -log u <= D = exp(z/T - best) <= exp(vm/T - best);
-// as -log u >= 1 - u, an element with 1 - u > D cannot, and for u on the
-// lattice (2k + 1) 2^-24 (k = word >> 9) that is k < (2^24 - 1 - D 2^24) / 2.
-// Those are skipped without the logarithms (one below the bound, for the
-// rounding of D); the others are scored as usual.
-template <int VEC>
-__device__ __forceinline__ void score_vec(const float (&x)[VEC], float vm, int32_t base, float invT,
+// Element q of a 16-byte vector (q known at compile time after unrolling).
+template <typename E>
+__device__ __forceinline__ float elt_of(uint4 v, int q)
+{
+    if constexpr (E::BYTES == 2) {
+        const uint32_t w = (q >> 1) == 0 ? v.x : ((q >> 1) == 1 ? v.y : ((q >> 1) == 2 ? v.z : v.w));
+        return (q & 1) ? bf_hi(w) : bf_lo(w);
+    } else {
+        return __uint_as_float(q == 0 ? v.x : (q == 1 ? v.y : (q == 2 ? v.z : v.w)));
+    }
+}
+
+// Scores of the elements of the 16-byte vector v starting at element
+// `base`, a multiple of 4 (the vector covers whole Philox blocks), whose
+// largest value is vm.  An element can only reach `best` if its Gumbel
+// noise -log(-log u) reaches best - z/T, i.e. -log u <= D = exp(z/T - best)
+// <= exp(vm/T - best); as -log u >= 1 - u, an element with 1 - u > D cannot,
+// and for u on the lattice (2k + 1) 2^-24 (k = word >> 9) that is
+// k < (2^24 - 1 - D 2^24) / 2.  Those are skipped without the logarithms
+// (one below the bound, for the rounding of D); the others are scored as
+// usual.  The values stay packed until an element is scored: fewer live
+// registers across the Philox rounds.
+template <typename E>
+__device__ __forceinline__ void score_vec(uint4 v, float vm, int32_t base, float invT,
                                           const Noise &nz, float &best, int32_t &bi)
 {
     const float D = ex2((vm * invT - best) * kLog2e);
@@ -404,14 +418,14 @@ __device__ __forceinline__ void score_vec(const float (&x)[VEC], float vm, int32
     // block's largest word passes over the usual block with nothing to score
     const uint32_t wthr = kthr << 9;
 #pragma unroll
-    for (int h = 0; h < VEC / 4; ++h) {
+    for (int h = 0; h < E::VEC / 4; ++h) {
         const uint4 w = nz.block((static_cast<uint32_t>(base) >> 2) + h);
         if (max(max(w.x, w.y), max(w.z, w.w)) < wthr) continue;
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             if (ws[j] >= wthr)
-                keep_best(fmaf(x[4 * h + j], invT, gumbel_of(ws[j])), base + 4 * h + j, best, bi);
+                keep_best(fmaf(elt_of<E>(v, 4 * h + j), invT, gumbel_of(ws[j])), base + 4 * h + j, best, bi);
     }
 }
 

@@ -383,12 +383,12 @@ __device__ void summary_sampler(const VerifyParams &p, const RowInfo &info, cons
             const uint4 v = body[i];
             const float vm = E::vmax(v);
             if (!(vm >= skip)) continue;
-            float x[VEC];
-            E::unpack(v, x);
             const int32_t base = g.a0 + i * VEC;
             if (whole_blocks) {
-                score_vec<VEC>(x, vm, base, invT, nz, best, bi);
+                score_vec<E>(v, vm, base, invT, nz, best, bi);
             } else {
+                float x[VEC];
+                E::unpack(v, x);
 #pragma unroll
                 for (int q = 0; q < VEC; ++q) keep_best(nz.score(x[q], base + q, invT), base + q, best, bi);
             }
