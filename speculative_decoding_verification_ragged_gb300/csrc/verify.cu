@@ -818,7 +818,9 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
         return;
     }
     griddep_wait();                        // the stream kernel's stores are visible
-    if (tid == 0) {
+    if (tid == 32) {
+        // the row record, by another warp than the one issuing the copies
+        // below (its loads would hold them back)
         if (MODE != MODE_CONF) {
             sh.info = reinterpret_cast<const RowInfo *>(p.ws_info)[r];
             sh.info.valid = sh.info.valid && r < min(__ldg(p.cu_rows + p.B), p.R_cap);
@@ -827,6 +829,8 @@ __global__ void __launch_bounds__(kThreads, 5) finish_rows_kernel(const VerifyPa
             inf.b = r; inf.valid = 1;
             sh.info = inf;
         }
+    }
+    if (tid == 0) {
         sh.ph[0] = sh.ph[1] = 0u;
         sh.timeout = 0;
         mbar_init(&sh.mbar[0], 1);
