@@ -15,14 +15,14 @@
 //     (the row is read from HBM exactly once; unaligned head / tail
 //     elements use plain loads); many short CTAs per SM keep the copies in
 //     flight and hide each other's latencies.  While the copy is in flight,
-//     warp 0 computes the row record (the sampler copies it from the
-//     records kernel): the owner request (32-way search of
-//     cu_rows), the row's position and validity and the owner's parameters;
-//     with a confidence margin also whether the margin applies (position,
-//     generated-token count, a warp scan of the protected ids) and the
-//     draft's logit (NaN if not).  The row's first chunk stores the record
-//     for the finish.  Pass 1 takes two loops over
-//     the thread's 16-byte vectors: the maximum and the first vector holding
+//     warp 0 computes the row record (the sampler's CTAs of later chunks
+//     copy it from the records kernel): the owner request (32-way
+//     search of cu_rows), the row's position and validity and the owner's
+//     parameters; with a confidence margin also whether the margin applies
+//     (position, generated-token count, a warp scan of the protected ids)
+//     and the draft's logit (NaN if not).  Outside the sampler the row's
+//     first chunk stores the record for the finish.  Pass 1 takes two loops
+//     over the thread's 16-byte vectors: the maximum and the first vector holding
 //     it (selects only), then sum exp(z - max) against it (packed f32x2
 //     arithmetic for bf16) and, for relaxed top-K, the count of logits above
 //     the draft's; warp reductions (redux.sync) and a CTA reduction give the
@@ -149,19 +149,20 @@ static_assert(Rec<Elt<uint16_t>>::BYTES % 16 == 0 && Rec<Elt<float>>::BYTES % 16
 
 // ------------------------------------------------- sampler records -----
 // Sampler only: one warp per packed row writes its row record (row_record)
-// before the stream kernel needs it.
-// (The other modes' stream CTAs compute their own record while their copy
-// is in flight: there it costs less than this launch and its wait, while
-// the sampler's record, with its parameter loads, costs its stream CTAs
-// more.)
+// for the stream CTAs of later chunks and for the finish.
+// (The other modes' stream CTAs all compute their own record while their
+// copy is in flight; for the sampler, with its parameter loads, that costs
+// its later CTAs more than this launch, while its first-chunk CTAs, whose
+// copies take long anyway in the first wave, would otherwise wait for it.)
 template <typename TIn>
 __global__ void __launch_bounds__(256) sample_records_kernel(const VerifyParams p)
 {
     // Launched as a programmatic dependent of whatever kernel precedes the
     // call (the previous call's finish, say), so its CTAs are resident when
     // that one ends.  Nothing is read before that kernel has completed, and
-    // the stream kernel is released only then: its chunk copies read the
-    // logits before it waits for this kernel.
+    // the stream kernel is released only then: its chunk copies (and its
+    // first chunks' own row records) read the call's inputs without waiting
+    // for this kernel.
     griddep_wait();
     griddep_launch_dependents();
     const int r = (blockIdx.x * 256 + threadIdx.x) >> 5;
@@ -444,6 +445,14 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
     }
     const TIn *row = reinterpret_cast<const TIn *>(p.logits) + static_cast<int64_t>(r) * p.ld;
     const ChunkGeom g = chunk_geom<E>(row, c, p.V);
+    // The sampler's first-chunk CTAs (chunk-major order puts them in the
+    // grid's first wave) compute their row's record themselves while their
+    // copy is in flight: the records kernel runs beside them, its loads
+    // queued behind their copies, and waiting for it would hold the whole
+    // first wave.  Later CTAs copy the record it wrote.  (Every CTA reads
+    // only the call's inputs, visible since the records kernel, whose
+    // launch released this grid, waited for the kernel before the call.)
+    const bool own_rec = MODE == MODE_SAMPLE && c == 0;
 
     if (tid == 0) {
         // The logits buffer holds R_cap rows, so the chunk copy is issued
@@ -452,12 +461,12 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
         mbar_init(&sh.mbar[0], 1);
         fence_mbar_init();
         const uint32_t bytes = static_cast<uint32_t>(g.nb) * 16u;
-        mbar_arrive_expect_tx(&sh.mbar[0], bytes + (MODE == MODE_SAMPLE ? 64u : 0u));
+        mbar_arrive_expect_tx(&sh.mbar[0], bytes + ((MODE == MODE_SAMPLE && !own_rec) ? 64u : 0u));
         // (with no body and no record the arrival alone completes the phase)
         if (bytes) bulk_g2s_stream(smem, row + g.a0, bytes, &sh.mbar[0]);
         int32_t R = p.n_rows;
         if (MODE != MODE_CONF) R = __ldg(p.cu_rows + p.B);
-        if (MODE == MODE_SAMPLE) {
+        if (MODE == MODE_SAMPLE && !own_rec) {
             griddep_wait();                 // the sampler's row records
             bulk_g2s(&sh.info, reinterpret_cast<const RowInfo *>(p.ws_info) + r, 64u, &sh.mbar[0]);
         }
@@ -468,13 +477,14 @@ __global__ void __launch_bounds__(kThreads, MODE == MODE_SAMPLE ? 5 : 6)
         }
         sh.R = min(R, p.R_cap);
     }
-    if (HAS_INFO && MODE != MODE_SAMPLE && tid < 32) {
+    if (HAS_INFO && (MODE != MODE_SAMPLE || own_rec) && tid < 32) {
         // the row record (owner request, position, parameters) while the
-        // copy is in flight; the row's first chunk stores it for the finish
+        // copy is in flight; outside the sampler the row's first chunk
+        // stores it for the finish (the sampler's records kernel does)
         const RowInfo inf = row_record<TIn, MODE>(p, r);
         if (tid == 0) {
             sh.info = inf;
-            if (c == 0) reinterpret_cast<RowInfo *>(p.ws_info)[r] = inf;
+            if (MODE != MODE_SAMPLE && c == 0) reinterpret_cast<RowInfo *>(p.ws_info)[r] = inf;
         }
     }
     float xe = -INFINITY;
