@@ -103,8 +103,8 @@ __device__ __forceinline__ void bad_request_outputs(const VerifyParams &p, int b
 }
 
 // The row record of packed row r, computed by one full warp (every lane
-// returns it): the owner request (largest b with cu_rows[b] <= r, a 32-way
-// search), position, validity and the owner's parameters.  With a
+// returns it): the owner request (largest b with cu_rows[b] <= r), position,
+// validity and the owner's parameters.  With a
 // confidence margin it also decides whether the margin applies to the row
 // (position, generated-token count, a warp scan of the protected ids) and
 // records the draft's logit (NaN if not); relaxed top-K records the draft's
@@ -118,24 +118,77 @@ __device__ RowInfo row_record(const VerifyParams &p, int r)
     inf.sel = 0; inf.bad = 0; inf.zd = INFINITY; inf.K = 1;
     inf.T = 0.f; inf.top_k = 0; inf.top_p = 1.f; inf.min_p = 0.f;
     inf.seed_lo = inf.seed_hi = inf.rid = 0;
-    int lo = 0, hi = p.B - 1;
-    while (hi > lo) {
-        const int step = (hi - lo + 31) / 32;
-        const int idx = min(lo + lane * step, hi);
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, __ldg(p.cu_rows + idx) <= r);
-        const int L = m ? 31 - __clz(m) : 0;
-        const int nlo = min(lo + L * step, hi);
-        const int nhi = (L == 31) ? hi : min(lo + (L + 1) * step - 1, hi);
-        lo = nlo;
-        hi = nhi;
+    inf.draft = __ldg(p.draft_ids + r);
+    // The owner: the largest b < B with cu_rows[b] <= r.  Outside the
+    // sampler, for 33 to 159 requests, the warp loads all of cu_rows[0..B]
+    // at once (lane l holds entries l*P .. l*P+P-1); when they are
+    // non-decreasing, b is the count of entries <= r less one and the range
+    // ends come by shuffles: one round of loads where the search below
+    // takes two.  Otherwise (the sampler, whose stream kernel measured
+    // slower with it; up to 32 requests, one round of the search anyway;
+    // more requests; offsets out of order) a 32-way search narrows
+    // [0, B-1] round by round.
+    int b = -1;
+    int32_t c0 = 0, rb = 0, re = 0;
+    if (MODE != MODE_SAMPLE && p.B > 32 && p.B <= 159) {
+        constexpr int kPer = 5;
+        const int P = (p.B + 1 + 31) / 32;
+        int32_t v[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int idx = lane * P + j;
+            v[j] = (j < P && idx <= p.B) ? __ldg(p.cu_rows + idx) : INT_MAX;
+        }
+        int cnt = 0;
+        bool mono = true;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int idx = lane * P + j;
+            if (j < P && idx < p.B && v[j] <= r) ++cnt;
+            if (j + 1 < kPer && j + 1 < P && v[j] > v[j + 1]) mono = false;
+        }
+        // the next lane's first entry continues this lane's last
+        int32_t last = v[0];
+#pragma unroll
+        for (int j = 1; j < kPer; ++j)
+            if (j < P) last = v[j];
+        const int32_t next_first = __shfl_down_sync(0xFFFFFFFFu, v[0], 1);
+        if (lane < 31 && last > next_first) mono = false;
+        if (__all_sync(0xFFFFFFFFu, mono)) {
+            b = max(__reduce_add_sync(0xFFFFFFFFu, cnt) - 1, 0);
+            // entries b and b + 1 (b + 1 <= B): lane and slot of each
+            int32_t sb = v[0], se = v[0];
+#pragma unroll
+            for (int j = 1; j < kPer; ++j) {
+                if (j == b % P) sb = v[j];
+                if (j == (b + 1) % P) se = v[j];
+            }
+            c0 = __shfl_sync(0xFFFFFFFFu, v[0], 0);
+            rb = __shfl_sync(0xFFFFFFFFu, sb, b / P);
+            re = __shfl_sync(0xFFFFFFFFu, se, (b + 1) / P);
+        }
     }
-    const int b = lo;
-    const int32_t c0 = __ldg(p.cu_rows), rb = __ldg(p.cu_rows + b), re = __ldg(p.cu_rows + b + 1);
+    if (b < 0) {
+        int lo = 0, hi = p.B - 1;
+        while (hi > lo) {
+            const int step = (hi - lo + 31) / 32;
+            const int idx = min(lo + lane * step, hi);
+            const unsigned m = __ballot_sync(0xFFFFFFFFu, __ldg(p.cu_rows + idx) <= r);
+            const int L = m ? 31 - __clz(m) : 0;
+            const int nlo = min(lo + L * step, hi);
+            const int nhi = (L == 31) ? hi : min(lo + (L + 1) * step - 1, hi);
+            lo = nlo;
+            hi = nhi;
+        }
+        b = lo;
+        c0 = __ldg(p.cu_rows);
+        rb = __ldg(p.cu_rows + b);
+        re = __ldg(p.cu_rows + b + 1);
+    }
     inf.b = b;
     inf.pos = r - rb;
     inf.k_b = re - rb - 1;
     inf.valid = (c0 == 0 && rb <= r && r < re && inf.k_b >= 0 && inf.k_b <= p.k_max && re <= p.R_cap);
-    inf.draft = __ldg(p.draft_ids + r);
     if (MODE == MODE_SAMPLE) {
         float T = __ldg(p.temperature + b), tp = __ldg(p.top_p + b), mp = __ldg(p.min_p + b);
         int32_t tk = __ldg(p.top_k + b);

@@ -82,6 +82,30 @@ def test_greedy_invalid_requests_set_status():
     assert_requests_equal(got, ref)
 
 
+@pytest.mark.parametrize("B", [33, 40, 159, 160])
+def test_owner_search_request_counts(B):
+    """Row owners for request counts around the one-round search of all
+    offsets (33 to 159 requests) and the round-by-round search above it,
+    with ragged lengths."""
+    sv = need_gpu()
+    vb = W.ragged_batch(seed=B, B=B, k_max=4, V=3000, dtype="bf16")
+    check_greedy(sv, vb)
+
+
+def test_owner_search_invalid_requests():
+    """40 requests (one round of offset loads) with an empty request and an
+    over-long one: non-decreasing offsets, invalid ranges."""
+    sv = need_gpu()
+    vb = W.ragged_batch(seed=41, B=40, k_max=2, V=500, dtype="f32", k_values=np.full(40, 2))
+    n = np.full(40, 3)
+    n[5], n[9] = 0, 6                                       # empty; k = 5 > k_max
+    vb.cu_rows[:] = np.concatenate([[0], np.cumsum(n)])
+    ref = oracle.verify_greedy(vb.logits, vb.dtype, vb.V, vb.B, vb.k_max, vb.cu_rows, vb.draft_ids)
+    got = host(run_greedy(sv, vb))
+    assert got["status"][0] & 0x10 and ref.status & 0x10
+    assert_requests_equal(got, ref)
+
+
 def test_greedy_without_row_outputs_and_repeat_calls():
     """Optional row outputs may be NULL; the workspace tickets return to zero
     so one workspace serves back-to-back calls."""
