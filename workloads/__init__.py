@@ -16,7 +16,9 @@ batch 16-256, 4-7 draft tokens):
   (vocabulary 152064), B128, gamma 4, relaxed top-K acceptance.
 
 The page workloads run real models on datasets that are not available here;
-these synthetic logits stand in for them (see the design doc for the recipe).
+these synthetic logits stand in for them: seeded N(0, sigma) rows of the
+pages' shapes, with the planted peaks, draft rules and parameter mixes each
+generator below states.
 
 Logits are produced in fp32 and, for bf16 rows, rounded to bf16 with
 round-to-nearest-even; the bf16 *bit patterns* (uint16) are what both sides
